@@ -1,0 +1,224 @@
+/*
+ * autosage.h -- C ABI of the GB300 (sm_103a) CSR sparse-aggregation library.
+ *
+ * Operations follow AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN
+ * Aggregation (SpMM/SDDMM) and CSR Attention" (Abstract): CSR SpMM, SDDMM,
+ * and the CSR attention pipeline SDDMM -> row-softmax -> SpMM, each run by
+ * a schedule that an input-aware planner picks with a cost estimate refined
+ * by on-device micro-probes and keeps in a persistent cache for
+ * deterministic replay. The graph interface follows the benchmark page
+ * "fused sparse attention-value aggregation" (problem statement): rows are
+ * destination nodes, row_ptr has n_rows + 1 int32 entries, col_idx holds
+ * each edge's source node, an edgeless row produces zeros.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named in an autosage_csr and every feature/output pointer are
+ *    DEVICE pointers owned by the caller; the library never frees them.
+ *  - Dense matrices are row-major with a leading dimension (elements) >= the
+ *    row width. Attention tensors are [n, heads, D], contiguous.
+ *  - Indices are int32; all offsets are formed in 64-bit inside kernels.
+ *  - Outputs are overwritten, never accumulated into.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Every op is asynchronous on it, except where stated.
+ *  - Argument errors are detected on the host before any launch and return
+ *    a status; nothing is launched then. A failed launch returns
+ *    AUTOSAGE_ERR_CUDA. autosage_last_error() gives a message for the
+ *    calling thread's last failure.
+ *  - The library allocates device memory only for plan workspace (owned by
+ *    the plan, freed by autosage_plan_destroy) and, where stated, for
+ *    stream-ordered temporaries released before the call's work completes.
+ */
+#ifndef AUTOSAGE_H
+#define AUTOSAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  AUTOSAGE_OK = 0,
+  AUTOSAGE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld < width, misalignment */
+  AUTOSAGE_ERR_INVALID_CSR = 2,   /* row_ptr not monotone / col_idx out of range (checked modes) */
+  AUTOSAGE_ERR_UNSUPPORTED = 3,   /* shape outside what a kernel handles (e.g. width too large) */
+  AUTOSAGE_ERR_CUDA = 4,          /* a CUDA call or launch failed */
+  AUTOSAGE_ERR_CACHE_IO = 5,      /* cache file cannot be opened / written */
+  AUTOSAGE_ERR_CACHE_FORMAT = 6,  /* cache file has a bad header or bad lines (good lines still load) */
+  AUTOSAGE_ERR_PROBE = 7,         /* every probed candidate failed; the default schedule is used */
+  AUTOSAGE_ERR_PLAN_MISMATCH = 8  /* plan built for another graph, op, width or dtype */
+} autosage_status;
+
+typedef enum { AUTOSAGE_F32 = 0, AUTOSAGE_BF16 = 1 } autosage_dtype;
+
+typedef enum {
+  AUTOSAGE_OP_SPMM = 0,          /* Y = A X */
+  AUTOSAGE_OP_SPMM_T = 1,        /* Y = A^T X (plan holds the transposed CSR) */
+  AUTOSAGE_OP_SDDMM = 2,         /* S = alpha * (Q K^T) sampled on A's pattern */
+  AUTOSAGE_OP_ATTN = 3,          /* fused CSR attention */
+  AUTOSAGE_OP_ATTN_UNFUSED = 4,  /* SDDMM -> row softmax -> SpMM with scores in HBM */
+  AUTOSAGE_OP_SOFTMAX = 5        /* per-row softmax of edge scores */
+} autosage_op;
+
+/* Schedule families the planner chooses among (all are this library's own kernels). */
+typedef enum {
+  AUTOSAGE_SCHED_AUTO = -1,      /* let the planner decide */
+  AUTOSAGE_SCHED_ROWGROUP = 0,   /* one lane group per row: G feature lanes x E edge lanes */
+  AUTOSAGE_SCHED_SPLIT = 1,      /* rows longer than `split` edges are cut into chunks whose
+                                    partial results are combined in a fixed order */
+  AUTOSAGE_SCHED_MERGEPATH = 2   /* equal (rows + edges) share per warp along the merge path,
+                                    carry-out of rows cut at warp boundaries, fixed-order fix-up */
+} autosage_sched_kind;
+
+typedef struct {
+  int kind;        /* autosage_sched_kind */
+  int lanes_f;     /* G: lanes across the feature vector (power of two, 1..32); 0 = auto */
+  int lanes_e;     /* E: lanes across edges of one row (power of two, G*E <= 32); 0 = auto */
+  int split;       /* SPLIT: chunk length in edges; MERGEPATH: items per warp; 0 = auto */
+} autosage_schedule;
+
+/* A CSR matrix in device memory. Rows are destinations, col_idx are sources.
+ * vals may be NULL (every edge value is 1). nnz must equal row_ptr[n_rows]. */
+typedef struct {
+  int64_t n_rows;
+  int64_t n_cols;
+  int64_t nnz;
+  const int32_t *row_ptr; /* [n_rows + 1] */
+  const int32_t *col_idx; /* [nnz], each in [0, n_cols) */
+  const float *vals;      /* [nnz] or NULL */
+} autosage_csr;
+
+typedef struct autosage_plan_s *autosage_plan_t;
+
+/* Plan flags. */
+#define AUTOSAGE_PLAN_PROBE 1u     /* refine the estimate with on-device micro-probes */
+#define AUTOSAGE_PLAN_NO_CACHE 2u  /* neither read nor write the persistent cache */
+#define AUTOSAGE_PLAN_VERIFY 4u    /* spot-check each probed candidate against the default */
+
+/* ---------------------------------------------------------------- ops */
+
+/* SpMM (Abstract: "CSR SpMM"). transpose == 0: Y[i,:] = sum_p vals[p] * X[col_idx[p],:]
+ * for the n_rows rows of A; X has n_cols rows. transpose == 1: Y = A^T X, which needs a
+ * plan built for AUTOSAGE_OP_SPMM_T (it holds A^T); Y has n_cols rows, X has n_rows rows.
+ * dt is the type of X and Y (values, accumulation and softmax math are fp32).
+ * plan may be NULL (transpose == 0 only): the default row-group schedule runs. */
+autosage_status autosage_spmm(const autosage_csr *A, const void *X, int64_t ldx, void *Y,
+                              int64_t ldy, int64_t F, autosage_dtype dt, int transpose,
+                              autosage_plan_t plan, void *stream);
+
+/* SDDMM (Abstract: "SDDMM"): out[p] = alpha * <Q[row(p),:], K[col_idx[p],:]> for every
+ * edge p, written in CSR order as fp32 [nnz]. Edge values are not multiplied in.
+ * Q has n_rows rows, K has n_cols rows, both of width F and type dt. */
+autosage_status autosage_sddmm(const autosage_csr *A, const void *Q, int64_t ldq, const void *K,
+                               int64_t ldk, int64_t F, autosage_dtype dt, float alpha,
+                               float *out, autosage_plan_t plan, void *stream);
+
+/* Row softmax of edge scores in place (Abstract: "row-softmax"; benchmark page: the row
+ * maximum is subtracted first). scores is fp32 [nnz, heads]; each row and head is
+ * normalised over the row's edges. */
+autosage_status autosage_row_softmax(const autosage_csr *A, float *scores, int heads,
+                                     autosage_plan_t plan, void *stream);
+
+/* CSR attention (Abstract: "CSR attention pipeline (SDDMM -> row-softmax -> SpMM)"):
+ * per head h, s_p = scale * <Q[i,h,:], K[col_idx[p],h,:]>, w = softmax over row i,
+ * out[i,h,:] = sum_p w_p V[col_idx[p],h,:]. Q/K/V/out are [n, heads, D] of type dt.
+ * fused != 0: one pass per row with an online softmax; scores never reach HBM.
+ * fused == 0: SDDMM, softmax and SpMM kernels with an fp32 [nnz, heads] score array,
+ * taken from the plan's workspace, or (plan == NULL) stream-ordered memory freed
+ * on the same stream. Empty rows give zeros. A must be square-compatible: K and V
+ * have n_cols rows, Q and out have n_rows rows. */
+autosage_status autosage_csr_attention(const autosage_csr *A, const void *Q, const void *K,
+                                       const void *V, int heads, int64_t D, autosage_dtype dt,
+                                       float scale, void *out, int fused, autosage_plan_t plan,
+                                       void *stream);
+
+/* The benchmark page's op (fused softmax + aggregation with given scores): per head,
+ * w = softmax over row i of scores[p, h]; out[i,h,:] = sum_p w_p V[col_idx[p],h,:].
+ * scores is fp32 [nnz, heads]; V and out are [n, heads, D] of type dt. */
+autosage_status autosage_edge_softmax_aggregate(const autosage_csr *A, const float *scores,
+                                                const void *V, int heads, int64_t D,
+                                                autosage_dtype dt, void *out,
+                                                autosage_plan_t plan, void *stream);
+
+/* ---------------------------------------------------------------- planning */
+
+/* Build a plan for (A, op, F, heads, dt). For attention ops F is the head dimension D.
+ * Computes row statistics and a structure fingerprint on the GPU, looks the key up in
+ * the process-wide cache (unless AUTOSAGE_PLAN_NO_CACHE); on a miss scores candidate
+ * schedules with the cost estimate, and with AUTOSAGE_PLAN_PROBE times the best few on
+ * the device (on scratch buffers, never on caller data), keeps the fastest, and records
+ * it in the cache. Workspace (chunk lists, partial buffers, A^T) is allocated and built.
+ * SYNCHRONISES `stream`. Returns AUTOSAGE_ERR_PROBE (with a usable default plan in
+ * *out) if every probe failed. */
+autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, int heads,
+                              autosage_dtype dt, unsigned flags, autosage_plan_t *out,
+                              void *stream);
+
+/* Build a plan with an explicit schedule (no cache, no probes). SYNCHRONISES `stream`. */
+autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op op, int64_t F,
+                                            int heads, autosage_dtype dt,
+                                            const autosage_schedule *sched,
+                                            autosage_plan_t *out, void *stream);
+
+/* Free a plan and its workspace (synchronises the device). NULL is allowed. */
+autosage_status autosage_plan_destroy(autosage_plan_t plan);
+
+/* Write a one-line description of the plan's schedule into buf (always NUL-terminated). */
+autosage_status autosage_plan_describe(autosage_plan_t plan, char *buf, size_t len);
+
+/* The schedule a plan runs (kind, lanes, split) and its probe time in ms (or -1). */
+autosage_status autosage_plan_schedule(autosage_plan_t plan, autosage_schedule *sched,
+                                       double *probe_ms);
+
+/* ---------------------------------------------------------------- persistent cache */
+
+/* Merge entries from a cache file into the process-wide cache. Lines that do not parse
+ * are skipped and reported with AUTOSAGE_ERR_CACHE_FORMAT; good lines still load. */
+autosage_status autosage_cache_load(const char *path);
+/* Write the process-wide cache (entries sorted by key) to path, atomically replaced. */
+autosage_status autosage_cache_save(const char *path);
+/* Drop every cached entry. */
+autosage_status autosage_cache_clear(void);
+/* Number of cached entries. */
+int64_t autosage_cache_size(void);
+
+/* ---------------------------------------------------------------- graph utilities */
+
+/* Row statistics of A computed on the GPU (planner input). ints[40] and reals[2] are
+ * HOST arrays: ints = {n_rows, nnz, max deg, min deg, empty rows, sum deg^2,
+ * rows with deg > long_threshold, edges in them, 32 log2 buckets (bucket 0: deg 0,
+ * bucket b: 2^(b-1) <= deg < 2^b)}, reals = {mean degree, coefficient of variation}.
+ * SYNCHRONISES `stream`. */
+autosage_status autosage_row_stats(const autosage_csr *A, int64_t long_threshold, int64_t *ints,
+                                   double *reals, void *stream);
+
+/* 64-bit fingerprint of A's structure (order-independent sum of SplitMix64-mixed
+ * (index, value) words of row_ptr and col_idx); *out is a HOST pointer. SYNCHRONISES. */
+autosage_status autosage_fingerprint(const autosage_csr *A, uint64_t *out, void *stream);
+
+/* Full structural check of A on the GPU: row_ptr[0] == 0, non-decreasing,
+ * row_ptr[n_rows] == nnz, every col_idx in [0, n_cols). Returns AUTOSAGE_OK or
+ * AUTOSAGE_ERR_INVALID_CSR. SYNCHRONISES `stream`. */
+autosage_status autosage_validate_csr(const autosage_csr *A, void *stream);
+
+/* CSR of A^T by a stable counting sort on the GPU: row_ptr_t [n_cols + 1],
+ * col_idx_t [nnz] (original rows, increasing inside each new row), vals_t [nnz]
+ * (may be NULL; ignored if A->vals is NULL). Device outputs owned by the caller.
+ * Uses stream-ordered temporaries. */
+autosage_status autosage_csr_transpose(const autosage_csr *A, int32_t *row_ptr_t,
+                                       int32_t *col_idx_t, float *vals_t, void *stream);
+
+/* ---------------------------------------------------------------- misc */
+
+const char *autosage_status_string(autosage_status s);
+/* Message of the calling thread's last failed call ("" if none). */
+const char *autosage_last_error(void);
+/* Library version string. */
+const char *autosage_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AUTOSAGE_H */

@@ -1,0 +1,187 @@
+// Shared device helpers: vector fragments of fp32 / bf16 feature rows,
+// streaming loads of the CSR arrays, lane-group geometry, work items.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace autosage {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kBlock = 256;  // threads per block of the gather kernels
+
+// ---------------------------------------------------------------- lane groups
+//
+// A warp is cut into 32 / (G*E) groups; each group owns one work item (a row
+// or a chunk of a row). Inside a group, lane l = e*G + g: g in [0, G) walks
+// the feature vector in VW-element fragments (fragment c = g + k*G for
+// k < NV), e in [0, E) walks the item's edges (p = begin + e, e + E, ...).
+// Feature lanes are adjacent, so one gathered row is read by adjacent lanes.
+struct Lanes {
+  int G, E, GE;
+  int lane, g, e, slot;
+  unsigned group_mask;  // the GE lanes of this group
+  unsigned sub_mask;    // the G lanes of this group that share edge lane e
+  __device__ __forceinline__ Lanes(int G_, int E_) : G(G_), E(E_), GE(G_ * E_) {
+    lane = threadIdx.x & 31;
+    const int l = lane % GE;
+    g = l % G;
+    e = l / G;
+    slot = lane / GE;
+    group_mask = (GE == 32) ? FULL : (((1u << GE) - 1u) << (slot * GE));
+    sub_mask = (G == 32) ? FULL : (((1u << G) - 1u) << (slot * GE + e * G));
+  }
+  // Global index of this lane's group.
+  __device__ __forceinline__ int64_t group_index(int64_t block_base) const {
+    return (block_base + (threadIdx.x >> 5)) * (32 / GE) + slot;
+  }
+};
+
+// ---------------------------------------------------------------- loads
+
+__device__ __forceinline__ int ld_stream_i32(const int32_t *p) { return __ldcs(p); }
+__device__ __forceinline__ float ld_stream_f32(const float *p) { return __ldcs(p); }
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x = a (low half), .y = b
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// A fragment of VW consecutive elements of type T kept in its raw (packed)
+// form; get(i) widens element i to fp32.
+template <typename T, int VW> struct Frag;
+
+template <> struct Frag<float, 4> {
+  float4 r;
+  __device__ __forceinline__ void load(const float *p) { r = __ldg(reinterpret_cast<const float4 *>(p)); }
+  __device__ __forceinline__ float get(int i) const { return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w; }
+};
+template <> struct Frag<float, 2> {
+  float2 r;
+  __device__ __forceinline__ void load(const float *p) { r = __ldg(reinterpret_cast<const float2 *>(p)); }
+  __device__ __forceinline__ float get(int i) const { return i == 0 ? r.x : r.y; }
+};
+template <> struct Frag<float, 1> {
+  float r;
+  __device__ __forceinline__ void load(const float *p) { r = __ldg(p); }
+  __device__ __forceinline__ float get(int) const { return r; }
+};
+template <> struct Frag<__nv_bfloat16, 8> {
+  uint4 r;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const uint4 *>(p)); }
+  __device__ __forceinline__ float get(int i) const {
+    const uint32_t w = i < 2 ? r.x : i < 4 ? r.y : i < 6 ? r.z : r.w;
+    return (i & 1) ? bf16hi(w) : bf16lo(w);
+  }
+};
+template <> struct Frag<__nv_bfloat16, 4> {
+  uint2 r;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const uint2 *>(p)); }
+  __device__ __forceinline__ float get(int i) const {
+    const uint32_t w = i < 2 ? r.x : r.y;
+    return (i & 1) ? bf16hi(w) : bf16lo(w);
+  }
+};
+template <> struct Frag<__nv_bfloat16, 2> {
+  uint32_t r;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const unsigned int *>(p)); }
+  __device__ __forceinline__ float get(int i) const { return (i & 1) ? bf16hi(r) : bf16lo(r); }
+};
+template <> struct Frag<__nv_bfloat16, 1> {
+  uint32_t r;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+    r = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p)));
+  }
+  __device__ __forceinline__ float get(int) const { return __uint_as_float(r << 16); }
+};
+
+// Store VW fp32 values as type T (bf16: round to nearest even), streaming.
+template <typename T, int VW> __device__ __forceinline__ void store_frag(T *p, const float (&o)[VW]);
+
+template <> __device__ __forceinline__ void store_frag<float, 4>(float *p, const float (&o)[4]) {
+  __stcs(reinterpret_cast<float4 *>(p), make_float4(o[0], o[1], o[2], o[3]));
+}
+template <> __device__ __forceinline__ void store_frag<float, 2>(float *p, const float (&o)[2]) {
+  __stcs(reinterpret_cast<float2 *>(p), make_float2(o[0], o[1]));
+}
+template <> __device__ __forceinline__ void store_frag<float, 1>(float *p, const float (&o)[1]) { __stcs(p, o[0]); }
+template <> __device__ __forceinline__ void store_frag<__nv_bfloat16, 8>(__nv_bfloat16 *p, const float (&o)[8]) {
+  __stcs(reinterpret_cast<uint4 *>(p), make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                                                  pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7])));
+}
+template <> __device__ __forceinline__ void store_frag<__nv_bfloat16, 4>(__nv_bfloat16 *p, const float (&o)[4]) {
+  __stcs(reinterpret_cast<uint2 *>(p), make_uint2(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3])));
+}
+template <> __device__ __forceinline__ void store_frag<__nv_bfloat16, 2>(__nv_bfloat16 *p, const float (&o)[2]) {
+  __stcs(reinterpret_cast<unsigned int *>(p), pack_bf16(o[0], o[1]));
+}
+template <> __device__ __forceinline__ void store_frag<__nv_bfloat16, 1>(__nv_bfloat16 *p, const float (&o)[1]) {
+  *p = __float2bfloat16_rn(o[0]);
+}
+
+// fp32 workspace partials: kept in L2 (the fix-up reads them right after).
+template <int VW> __device__ __forceinline__ void store_partial(float *p, const float (&o)[VW]) {
+#pragma unroll
+  for (int i = 0; i < VW; ++i) __stcg(p + i, o[i]);
+}
+
+// ---------------------------------------------------------------- work items
+//
+// Rows whose degree is at most `split` are work items of their own. Longer
+// rows are cut into chunks of `split` edges; chunk c covers edges
+// [chunk_begin[c], min(chunk_begin[c] + split, row end)) of row chunk_row[c]
+// and writes its partial result at slot c. Long row j owns the consecutive
+// chunks [long_ptr[j], long_ptr[j+1]), so a fix-up combines them in order.
+struct ChunkList {
+  const int32_t *chunk_row = nullptr;    // [n_chunks]
+  const int32_t *chunk_begin = nullptr;  // [n_chunks]
+  const int32_t *long_rows = nullptr;    // [n_long]
+  const int32_t *long_ptr = nullptr;     // [n_long + 1]
+  int n_chunks = 0;
+  int n_long = 0;
+  int split = 0;  // 0: no row is cut
+};
+
+// Resolve the work item of a group: blocks [0, chunk_blocks) take chunks,
+// the rest take rows. Returns false (b == e) for idle groups and for rows
+// handled through chunks; such groups still take part in group shuffles.
+struct Item {
+  int64_t row;
+  int b, e;
+  int chunk;  // -1 for a whole row
+  bool active;
+};
+
+__device__ __forceinline__ Item resolve_item(const Lanes &L, int64_t n_rows, const int32_t *row_ptr,
+                                             const ChunkList &cl, int64_t chunk_blocks) {
+  Item it{0, 0, 0, -1, false};
+  const int64_t bid = blockIdx.x;
+  if (bid < chunk_blocks) {
+    const int64_t c = L.group_index(bid * (kBlock / 32)) ;
+    if (c < cl.n_chunks) {
+      it.chunk = static_cast<int>(c);
+      it.row = cl.chunk_row[c];
+      it.b = cl.chunk_begin[c];
+      const int re = row_ptr[it.row + 1];
+      it.e = (re - it.b > cl.split) ? it.b + cl.split : re;
+      it.active = true;
+    }
+  } else {
+    const int64_t r = L.group_index((bid - chunk_blocks) * (kBlock / 32));
+    if (r < n_rows) {
+      it.row = r;
+      it.b = row_ptr[r];
+      it.e = row_ptr[r + 1];
+      it.active = !(cl.split > 0 && it.e - it.b > cl.split);
+      if (!it.active) it.e = it.b;
+    }
+  }
+  return it;
+}
+
+__device__ __forceinline__ int64_t items_per_block(int GE) { return (kBlock / 32) * (32 / GE); }
+
+}  // namespace autosage

@@ -1,0 +1,98 @@
+// Internal launcher interface between the host runtime and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace autosage {
+
+enum class DType { F32 = 0, BF16 = 1 };
+
+inline int dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
+
+// Feature geometry of one launch: rows of F = H * D elements are read in
+// fragments of VW elements (VW * size = vector bytes); nfrag = F / VW;
+// cph = D / VW fragments per head; lanes G with NV fragments per lane.
+struct Geom {
+  DType dt;
+  int H = 1;
+  int64_t D = 0;
+  int VW = 1;
+  int nfrag = 0;
+  int cph = 0;
+  int G = 1;
+  int E = 1;
+  int NV = 1;
+  int mshift = 0;  // log2(slots per head group per lane)
+  int R = 1;       // lanes in one head reduction
+  int es = 1;      // elements between consecutive edges in per-edge arrays (vals, scores)
+};
+
+// SpMM over rows (and chunks of cut rows) with per-edge (per-head) weights.
+// vals: [nnz * H] or null. partial: [n_chunks * F] fp32 for chunk results.
+cudaError_t launch_spmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                        const int32_t *col_idx, const float *vals, const void *X, int64_t ldx,
+                        void *Y, int64_t ldy, const ChunkList &cl, float *partial,
+                        cudaStream_t s);
+
+// SDDMM: S[p*H + h] = alpha * <Q[row, h], K[col, h]>.
+cudaError_t launch_sddmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                         const int32_t *col_idx, const void *Q, int64_t ldq, const void *K,
+                         int64_t ldk, float alpha, float *S, const ChunkList &cl, cudaStream_t s);
+
+// Row softmax in place on S [nnz, H]. ml: [n_chunks * H * 2] fp32 workspace,
+// row_ml: [n_long * H * 2] fp32 workspace (only with cut rows).
+cudaError_t launch_row_softmax(int64_t n_rows, const int32_t *row_ptr, int H, float *S,
+                               const ChunkList &cl, float *ml, float *row_ml, cudaStream_t s);
+
+// Fused attention (scores from Q.K, or given scores when `scores` != null).
+// part_acc: [n_chunks * F], part_ml: [n_chunks * H * 2] fp32 workspace.
+cudaError_t launch_attention(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                             const int32_t *col_idx, const void *Q, const void *K,
+                             const float *scores, const void *V, int64_t ld, float scale,
+                             void *O, const ChunkList &cl, float *part_acc, float *part_ml,
+                             cudaStream_t s);
+
+// Merge-path SpMM: warp w covers diagonals [w*items, (w+1)*items) of the
+// (rows + edges) merge path; part: [n_warps + 1] int2 (row, edge) starts.
+// carry_val: [n_warps * F] fp32, carry_row: [n_warps] int32.
+cudaError_t launch_spmm_mergepath(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                                  const int32_t *col_idx, const float *vals, const void *X,
+                                  int64_t ldx, void *Y, int64_t ldy, const int2 *part,
+                                  int64_t n_warps, float *carry_val, int32_t *carry_row,
+                                  cudaStream_t s);
+cudaError_t launch_mergepath_partition(int64_t n_rows, int64_t nnz, const int32_t *row_ptr,
+                                       int64_t items, int64_t n_warps, int2 *part, cudaStream_t s);
+
+// ---- graph utilities (graph.cu)
+// stats: ints[40] (int64) and a double sum, device buffers.
+cudaError_t launch_row_stats(int64_t n_rows, const int32_t *row_ptr, int64_t long_threshold,
+                             unsigned long long *ints, cudaStream_t s);
+cudaError_t launch_fingerprint(int64_t n_rows, int64_t nnz, const int32_t *row_ptr,
+                               const int32_t *col_idx, unsigned long long *out, cudaStream_t s);
+cudaError_t launch_validate(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *row_ptr,
+                            const int32_t *col_idx, int *err, cudaStream_t s);
+// Exclusive scan of n int32 values into out[n + 1] (out[n] = total). tmp: scan_tmp_bytes(n).
+size_t scan_tmp_bytes(int64_t n);
+cudaError_t launch_exclusive_scan(const int32_t *in, int32_t *out, int64_t n, void *tmp,
+                                  cudaStream_t s);
+// Long-row chunk lists for `split`: flags/scan over rows. Writes n_long and n_chunks
+// to host (synchronises), allocating nothing; buffers sized by the caller from
+// upper bounds (n_rows + 1 and nnz / split + n_rows + 1).
+cudaError_t build_chunk_lists(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *flags,
+                              int32_t *scan_out, void *scan_tmp, int32_t *long_rows,
+                              int32_t *long_ptr, int32_t *chunk_row, int32_t *chunk_begin,
+                              int64_t *n_long_out, int64_t *n_chunks_out, cudaStream_t s);
+// Stable transpose by LSD radix sort; temporaries from cudaMallocAsync on s.
+cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *row_ptr,
+                          const int32_t *col_idx, const float *vals, int32_t *row_ptr_t,
+                          int32_t *col_idx_t, float *vals_t, cudaStream_t s);
+// Deterministic pseudo-random fill of probe buffers (values in [-1, 1)).
+cudaError_t fill_probe(void *p, int64_t n_elems, DType dt, uint64_t seed, cudaStream_t s);
+// Count elements with |a - b| > atol + rtol * |b| (fp32 or bf16 arrays) into *count (device).
+cudaError_t launch_compare(const void *a, const void *b, int64_t n, DType dt, float rtol,
+                           float atol, unsigned long long *count, cudaStream_t s);
+
+}  // namespace autosage

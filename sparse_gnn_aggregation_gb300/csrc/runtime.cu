@@ -1,0 +1,1302 @@
+// Host runtime and C ABI: argument checks, feature geometry, plans and their
+// workspace, the input-aware schedule picker (cost estimate from row
+// statistics, refined by on-device micro-probes), and the persistent plan
+// cache (AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN Aggregation
+// (SpMM/SDDMM) and CSR Attention", Abstract: "chooses tiling and mapping
+// per input using a lightweight estimate refined by on-device
+// micro-probes ... a persistent cache for deterministic replay"). The
+// fallback ("guardrail") is this library's own default row-group schedule,
+// never a vendor library or the CPU.
+#include <algorithm>
+#include <cinttypes>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <map>
+#include <mutex>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include "../../include/autosage.h"
+#include "internal.h"
+
+using namespace autosage;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+autosage_status fail(autosage_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+autosage_status cuda_fail(cudaError_t e, const char *where) {
+  return fail(AUTOSAGE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(expr)                                     \
+  do {                                                     \
+    cudaError_t _e = (expr);                               \
+    if (_e != cudaSuccess) return cuda_fail(_e, #expr);    \
+  } while (0)
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+int pow2ceil(int64_t x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+int log2i(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// ---------------------------------------------------------------- validation
+
+autosage_status check_csr(const autosage_csr *A, bool need_cols) {
+  if (!A) return fail(AUTOSAGE_ERR_INVALID_ARG, "A is NULL");
+  if (A->n_rows < 0 || A->n_cols < 0 || A->nnz < 0)
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "negative CSR size");
+  if (A->n_rows >= INT32_MAX || A->n_cols >= INT32_MAX || A->nnz >= INT32_MAX)
+    return fail(AUTOSAGE_ERR_UNSUPPORTED, "CSR sizes must fit int32");
+  if (!A->row_ptr) return fail(AUTOSAGE_ERR_INVALID_ARG, "row_ptr is NULL");
+  if (A->nnz > 0 && !A->col_idx) return fail(AUTOSAGE_ERR_INVALID_ARG, "col_idx is NULL");
+  if (A->nnz > 0 && A->n_cols == 0) return fail(AUTOSAGE_ERR_INVALID_CSR, "edges but no columns");
+  if ((reinterpret_cast<uintptr_t>(A->row_ptr) | reinterpret_cast<uintptr_t>(A->col_idx) |
+       reinterpret_cast<uintptr_t>(A->vals)) & 3u)
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "CSR arrays must be 4-byte aligned");
+  (void)need_cols;
+  if (getenv("AUTOSAGE_CHECK") && atoi(getenv("AUTOSAGE_CHECK")) > 0) {
+    // full structural check on the GPU (synchronising)
+    autosage_status st = autosage_validate_csr(A, nullptr);
+    if (st != AUTOSAGE_OK) return st;
+  }
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- geometry
+
+struct Mat {
+  const void *p;
+  int64_t ld;
+};
+
+// Pick the widest fragment (16, 8, 4 or 2 bytes) that every matrix's
+// pointer, leading dimension and the head width allow; then lanes and slots.
+autosage_status choose_geom(DType dt, int H, int64_t D, std::initializer_list<Mat> mats, int G_req,
+                            int E_req, bool need_head_reduce, int nv_max, Geom &g) {
+  const int s = dtype_size(dt);
+  const int64_t F = (int64_t)H * D;
+  int vb = 0;
+  for (int cand : {16, 8, 4, 2}) {
+    if (cand < s) continue;
+    if ((D * s) % cand) continue;
+    bool ok = true;
+    for (const Mat &m : mats) {
+      if ((reinterpret_cast<uintptr_t>(m.p) % cand) || ((m.ld * s) % cand)) ok = false;
+    }
+    if (ok) {
+      vb = cand;
+      break;
+    }
+  }
+  if (vb == 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "feature pointers must be aligned to the element size");
+  g.dt = dt;
+  g.H = H;
+  g.D = D;
+  g.es = H;
+  g.VW = vb / s;
+  g.nfrag = static_cast<int>(F / g.VW);
+  g.cph = static_cast<int>(D / g.VW);
+  g.G = G_req > 0 ? G_req : std::min(32, pow2ceil(g.nfrag));
+  if (!is_pow2(g.G) || g.G > 32) return fail(AUTOSAGE_ERR_INVALID_ARG, "lanes_f must be a power of two <= 32");
+  if (need_head_reduce && H > 1) {
+    if (!is_pow2(g.cph))
+      return fail(AUTOSAGE_ERR_UNSUPPORTED, "multi-head reduction needs D/VW a power of two");
+    // (both powers of two: one divides the other)
+  }
+  const int64_t per_lane = (g.nfrag + g.G - 1) / g.G;
+  g.NV = pow2ceil(per_lane);
+  if (g.NV > nv_max)
+    return fail(AUTOSAGE_ERR_UNSUPPORTED, "feature width %" PRId64 " too large for one pass", F);
+  g.E = E_req > 0 ? E_req : std::max(1, std::min(32 / g.G, 8));
+  if (!is_pow2(g.E) || g.G * g.E > 32) return fail(AUTOSAGE_ERR_INVALID_ARG, "lanes_f * lanes_e must be <= 32");
+  if (H == 1) {
+    g.mshift = log2i(g.NV);
+    g.R = g.G;
+  } else if (g.cph <= g.G) {
+    g.mshift = 0;
+    g.R = g.cph;
+  } else {
+    g.mshift = log2i(g.cph / g.G);
+    g.R = g.G;
+  }
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- device info
+
+struct DeviceInfo {
+  int device = -1;
+  int sms = 0;
+  std::string name;
+  double bw = 6.8e12;  // bytes/s used by the estimate
+};
+
+DeviceInfo device_info() {
+  DeviceInfo d;
+  cudaGetDevice(&d.device);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, d.device) == cudaSuccess) {
+    d.sms = prop.multiProcessorCount;
+    d.name = prop.name;
+    for (char &c : d.name)
+      if (c == ' ' || c == '|' || c == '\t') c = '_';
+  }
+  return d;
+}
+
+// ---------------------------------------------------------------- device buffers
+
+struct DevBuf {
+  void *p = nullptr;
+  size_t bytes = 0;
+  cudaError_t alloc(size_t n) {
+    release();
+    if (n == 0) return cudaSuccess;
+    cudaError_t e = cudaMalloc(&p, n);
+    if (e == cudaSuccess) bytes = n;
+    else p = nullptr;
+    return e;
+  }
+  void release() {
+    if (p) cudaFree(p);
+    p = nullptr;
+    bytes = 0;
+  }
+  template <typename T> T *as() const { return static_cast<T *>(p); }
+};
+
+// ---------------------------------------------------------------- statistics
+
+struct RowStats {
+  int64_t ints[40];
+  double mean = 0, cv = 0;
+};
+
+autosage_status gpu_row_stats(int64_t n_rows, const int32_t *row_ptr, int64_t thr, RowStats &out,
+                              cudaStream_t s) {
+  unsigned long long *d = nullptr;
+  CUDA_TRY(cudaMallocAsync(&d, 40 * sizeof(unsigned long long), s));
+  cudaError_t e = launch_row_stats(n_rows, row_ptr, thr, d, s);
+  unsigned long long h[40] = {0};
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h, d, sizeof h, cudaMemcpyDeviceToHost, s);
+  cudaFreeAsync(d, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "row statistics");
+  for (int i = 0; i < 40; ++i) out.ints[i] = static_cast<int64_t>(h[i]);
+  out.ints[0] = n_rows;
+  if (n_rows == 0) out.ints[3] = 0;
+  out.mean = n_rows > 0 ? (double)out.ints[1] / (double)n_rows : 0.0;
+  const double var = n_rows > 0 ? (double)out.ints[5] / (double)n_rows - out.mean * out.mean : 0.0;
+  out.cv = out.mean > 0.0 ? std::sqrt(var > 0.0 ? var : 0.0) / out.mean : 0.0;
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- plan
+
+struct Sched {
+  int kind = AUTOSAGE_SCHED_ROWGROUP;
+  int G = 0, E = 0, split = 0;
+};
+
+}  // namespace
+
+struct autosage_plan_s {
+  autosage_op op;
+  DType dt;
+  int64_t F;  // feature width (attention: head dim D)
+  int H;
+  int64_t n_rows, n_cols, nnz;
+  Sched sched;
+  double probe_ms = -1;
+  double est_ms = -1;
+  bool from_cache = false;
+  // the CSR the kernels walk (A, or A^T for SPMM_T)
+  int64_t k_rows = 0;
+  const int32_t *k_row_ptr = nullptr;
+  const int32_t *k_col_idx = nullptr;
+  const float *k_vals = nullptr;
+  DevBuf t_row_ptr, t_col_idx, t_vals;  // A^T when op == SPMM_T
+  // split workspace
+  DevBuf long_rows, long_ptr, chunk_row, chunk_begin, partial, ml, row_ml;
+  ChunkList cl;
+  // merge-path workspace
+  DevBuf mp_part, mp_carry_val, mp_carry_row;
+  int64_t mp_warps = 0;
+  // unfused attention scores
+  DevBuf scores;
+  ~autosage_plan_s() {
+    for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
+                      &chunk_begin, &partial, &ml, &row_ml, &mp_part, &mp_carry_val,
+                      &mp_carry_row, &scores})
+      b->release();
+  }
+};
+
+namespace {
+
+// ---------------------------------------------------------------- cache
+
+constexpr const char *kCacheHeader = "# autosage plan cache v1";
+
+struct CacheEntry {
+  Sched sched;
+  double probe_ms = -1;
+};
+
+std::mutex g_cache_mu;
+std::map<std::string, CacheEntry> g_cache;
+
+std::string cache_key(const DeviceInfo &dev, autosage_op op, DType dt, int64_t F, int H,
+                      int64_t n_rows, int64_t n_cols, int64_t nnz, uint64_t fp) {
+  char buf[512];
+  snprintf(buf, sizeof buf, "%s|sm%d|op%d|dt%d|F%" PRId64 "|H%d|n%" PRId64 "|m%" PRId64 "|nnz%" PRId64 "|fp%016" PRIx64,
+           dev.name.c_str(), dev.sms, (int)op, (int)dt, F, H, n_rows, n_cols, nnz, fp);
+  return buf;
+}
+
+const char *sched_name(int kind) {
+  switch (kind) {
+    case AUTOSAGE_SCHED_ROWGROUP: return "rowgroup";
+    case AUTOSAGE_SCHED_SPLIT: return "split";
+    case AUTOSAGE_SCHED_MERGEPATH: return "mergepath";
+  }
+  return "?";
+}
+
+// ---------------------------------------------------------------- op geometry
+
+struct OpShape {
+  int H;
+  int64_t D;       // width per head (F for H == 1)
+  bool head_reduce;
+  int nv_max;
+};
+
+OpShape op_shape(autosage_op op, int64_t F, int H) {
+  switch (op) {
+    case AUTOSAGE_OP_SPMM:
+    case AUTOSAGE_OP_SPMM_T: return {1, F, false, 16};
+    case AUTOSAGE_OP_SDDMM: return {1, F, true, 16};
+    case AUTOSAGE_OP_ATTN: return {H, F, true, 8};
+    case AUTOSAGE_OP_ATTN_UNFUSED: return {H, F, true, 16};
+    case AUTOSAGE_OP_SOFTMAX: return {H, 1, false, 16};
+  }
+  return {1, F, false, 16};
+}
+
+// Default schedule (the guardrail): row groups with lanes from the width.
+Sched default_sched() { return Sched{AUTOSAGE_SCHED_ROWGROUP, 0, 0, 0}; }
+
+// ---------------------------------------------------------------- workspace
+
+autosage_status build_split(autosage_plan_s *P, int split, cudaStream_t s) {
+  P->cl = ChunkList{};
+  if (split <= 0 || P->k_rows == 0) return AUTOSAGE_OK;
+  DevBuf flags, scan_out, scan_tmp;
+  CUDA_TRY(flags.alloc(sizeof(int32_t) * (size_t)(P->k_rows + 1)));
+  CUDA_TRY(scan_out.alloc(sizeof(int32_t) * (size_t)(P->k_rows + 1)));
+  CUDA_TRY(scan_tmp.alloc(scan_tmp_bytes(P->k_rows)));
+  CUDA_TRY(P->long_rows.alloc(sizeof(int32_t) * (size_t)(P->k_rows + 1)));
+  CUDA_TRY(P->long_ptr.alloc(sizeof(int32_t) * (size_t)(P->k_rows + 1)));
+  const int64_t max_chunks = P->nnz / split + P->k_rows + 1;
+  // chunk arrays sized after counting: first pass counts, second fills
+  int64_t n_long = 0, n_chunks = 0;
+  {
+    // temporary chunk arrays large enough for any graph would be wasteful; count first
+    RowStats st;
+    autosage_status rs = gpu_row_stats(P->k_rows, P->k_row_ptr, split, st, s);
+    if (rs != AUTOSAGE_OK) return rs;
+    n_chunks = (st.ints[7] + (int64_t)split - 1) / split + st.ints[6];  // upper bound
+    n_chunks = std::min(n_chunks, max_chunks);
+  }
+  CUDA_TRY(P->chunk_row.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(n_chunks, 1)));
+  CUDA_TRY(P->chunk_begin.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(n_chunks, 1)));
+  int64_t got_chunks = 0;
+  CUDA_TRY(build_chunk_lists(P->k_rows, P->k_row_ptr, split, flags.as<int32_t>(), scan_out.as<int32_t>(),
+                             scan_tmp.p, P->long_rows.as<int32_t>(), P->long_ptr.as<int32_t>(),
+                             P->chunk_row.as<int32_t>(), P->chunk_begin.as<int32_t>(), &n_long,
+                             &got_chunks, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  if (got_chunks > n_chunks) return fail(AUTOSAGE_ERR_CUDA, "chunk count exceeded its bound");
+  P->cl.chunk_row = P->chunk_row.as<int32_t>();
+  P->cl.chunk_begin = P->chunk_begin.as<int32_t>();
+  P->cl.long_rows = P->long_rows.as<int32_t>();
+  P->cl.long_ptr = P->long_ptr.as<int32_t>();
+  P->cl.n_long = static_cast<int>(n_long);
+  P->cl.n_chunks = static_cast<int>(got_chunks);
+  P->cl.split = split;
+  // partial buffers for every consumer of the chunk list
+  const int64_t C = got_chunks;
+  const int64_t width = P->F * (P->op == AUTOSAGE_OP_ATTN || P->op == AUTOSAGE_OP_ATTN_UNFUSED ? P->H : 1);
+  if (P->op != AUTOSAGE_OP_SDDMM && P->op != AUTOSAGE_OP_SOFTMAX)
+    CUDA_TRY(P->partial.alloc(sizeof(float) * (size_t)std::max<int64_t>(C * width, 1)));
+  const int Hs = (P->op == AUTOSAGE_OP_SOFTMAX || P->op == AUTOSAGE_OP_ATTN ||
+                  P->op == AUTOSAGE_OP_ATTN_UNFUSED) ? P->H : 1;
+  CUDA_TRY(P->ml.alloc(sizeof(float) * (size_t)std::max<int64_t>(C * Hs * 2 + C, 1)));
+  CUDA_TRY(P->row_ml.alloc(sizeof(float) * (size_t)std::max<int64_t>(n_long * Hs * 2, 1)));
+  return AUTOSAGE_OK;
+}
+
+autosage_status build_mergepath(autosage_plan_s *P, int items, int64_t width, cudaStream_t s) {
+  const int64_t total = P->k_rows + P->nnz;
+  P->mp_warps = (total + items - 1) / items;
+  CUDA_TRY(P->mp_part.alloc(sizeof(int2) * (size_t)(P->mp_warps + 1)));
+  CUDA_TRY(P->mp_carry_val.alloc(sizeof(float) * (size_t)std::max<int64_t>(P->mp_warps * width, 1)));
+  CUDA_TRY(P->mp_carry_row.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(P->mp_warps, 1)));
+  CUDA_TRY(launch_mergepath_partition(P->k_rows, P->nnz, P->k_row_ptr, items, P->mp_warps,
+                                      P->mp_part.as<int2>(), s));
+  return AUTOSAGE_OK;
+}
+
+// Build the workspace of a schedule for plan P (P->sched set).
+autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
+  for (DevBuf *b : {&P->long_rows, &P->long_ptr, &P->chunk_row, &P->chunk_begin, &P->partial,
+                    &P->ml, &P->row_ml, &P->mp_part, &P->mp_carry_val, &P->mp_carry_row})
+    b->release();
+  P->cl = ChunkList{};
+  P->mp_warps = 0;
+  autosage_status st = AUTOSAGE_OK;
+  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT) {
+    st = build_split(P, P->sched.split, s);
+  } else if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
+    if (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)
+      return fail(AUTOSAGE_ERR_UNSUPPORTED, "merge-path schedule is SpMM only");
+    st = build_mergepath(P, P->sched.split, P->F, s);
+  }
+  if (st != AUTOSAGE_OK) return st;
+  if (P->op == AUTOSAGE_OP_ATTN_UNFUSED && !P->scores.p)
+    CUDA_TRY(P->scores.alloc(sizeof(float) * (size_t)std::max<int64_t>(P->nnz * P->H, 1)));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- running ops
+
+struct OpArgs {
+  const void *X = nullptr;  // SpMM input / attention V
+  int64_t ldx = 0;
+  void *Y = nullptr;        // SpMM output / attention out
+  int64_t ldy = 0;
+  const void *Q = nullptr, *K = nullptr;
+  int64_t ldq = 0, ldk = 0;
+  float alpha = 1.f;
+  float *S = nullptr;       // SDDMM output / softmax in-out
+  const float *given = nullptr;  // given scores (edge-softmax aggregation)
+};
+
+// Run `op` with plan P's schedule (plan-free runs use a transient P with
+// the default schedule and no workspace).
+autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a, cudaStream_t s) {
+  const ChunkList &cl = P->cl;
+  const OpShape sh = op_shape(op, P->F, P->H);
+  Geom g;
+  autosage_status st;
+  cudaError_t e = cudaSuccess;
+  switch (op) {
+    case AUTOSAGE_OP_SPMM:
+    case AUTOSAGE_OP_SPMM_T: {
+      st = choose_geom(P->dt, 1, P->F, {{a.X, a.ldx}, {a.Y, a.ldy}}, P->sched.G,
+                       P->sched.kind == AUTOSAGE_SCHED_MERGEPATH
+                           ? 0 : P->sched.E, false, 16, g);
+      if (st != AUTOSAGE_OK) return st;
+      if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
+        g.E = 32 / g.G;
+        e = launch_spmm_mergepath(g, P->k_rows, P->k_row_ptr, P->k_col_idx, P->k_vals, a.X, a.ldx,
+                                  a.Y, a.ldy, P->mp_part.as<int2>(), P->mp_warps,
+                                  P->mp_carry_val.as<float>(), P->mp_carry_row.as<int32_t>(), s);
+      } else {
+        e = launch_spmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, P->k_vals, a.X, a.ldx, a.Y, a.ldy,
+                        cl, P->partial.as<float>(), s);
+      }
+      break;
+    }
+    case AUTOSAGE_OP_SDDMM: {
+      st = choose_geom(P->dt, 1, P->F, {{a.Q, a.ldq}, {a.K, a.ldk}}, P->sched.G, P->sched.E, true, 16, g);
+      if (st != AUTOSAGE_OK) return st;
+      e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.ldq, a.K, a.ldk, a.alpha, a.S, cl, s);
+      break;
+    }
+    case AUTOSAGE_OP_SOFTMAX: {
+      e = launch_row_softmax(P->k_rows, P->k_row_ptr, P->H, a.S, cl, P->ml.as<float>(),
+                             P->row_ml.as<float>(), s);
+      break;
+    }
+    case AUTOSAGE_OP_ATTN: {
+      const int64_t ld = P->H * P->F;
+      if (a.given) {
+        st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, P->sched.G, P->sched.E, false, 8, g);
+      } else {
+        st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}, {a.X, ld}, {a.Y, ld}}, P->sched.G,
+                         P->sched.E, true, 8, g);
+      }
+      if (st == AUTOSAGE_OK) {
+        e = launch_attention(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.K, a.given, a.X, ld, a.alpha,
+                             a.Y, cl, P->partial.as<float>(), P->ml.as<float>(), s);
+        break;
+      }
+      if (st != AUTOSAGE_ERR_UNSUPPORTED || P->H == 1) return st;
+      // heads whose fragments cannot share an aligned lane segment: one launch per head
+      const size_t es = dtype_size(P->dt);
+      for (int h = 0; h < P->H && e == cudaSuccess; ++h) {
+        const int64_t off = (int64_t)h * P->F;
+        auto at = [&](const void *p) { return p ? static_cast<const char *>(p) + off * es : nullptr; };
+        st = choose_geom(P->dt, 1, P->F, {{at(a.Q), ld}, {at(a.K), ld}, {at(a.X), ld}, {at(a.Y), ld}},
+                         P->sched.G, P->sched.E, true, 8, g);
+        if (st != AUTOSAGE_OK) return st;
+        g.es = P->H;
+        e = launch_attention(g, P->k_rows, P->k_row_ptr, P->k_col_idx, at(a.Q), at(a.K),
+                             a.given ? a.given + h : nullptr, at(a.X), ld, a.alpha,
+                             const_cast<char *>(at(a.Y)), cl, P->partial.as<float>(), P->ml.as<float>(), s);
+      }
+      break;
+    }
+    case AUTOSAGE_OP_ATTN_UNFUSED: {
+      const int64_t ld = P->H * P->F;
+      float *S = a.S;
+      st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}}, P->sched.G, P->sched.E, true, 16, g);
+      if (st == AUTOSAGE_OK) {
+        e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, ld, a.K, ld, a.alpha, S, cl, s);
+      } else if (st == AUTOSAGE_ERR_UNSUPPORTED && P->H > 1) {
+        const size_t es = dtype_size(P->dt);
+        for (int h = 0; h < P->H && e == cudaSuccess; ++h) {
+          const char *q = static_cast<const char *>(a.Q) + (int64_t)h * P->F * es;
+          const char *k = static_cast<const char *>(a.K) + (int64_t)h * P->F * es;
+          st = choose_geom(P->dt, 1, P->F, {{q, ld}, {k, ld}}, P->sched.G, P->sched.E, true, 16, g);
+          if (st != AUTOSAGE_OK) return st;
+          g.es = P->H;
+          e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, q, ld, k, ld, a.alpha, S + h, cl, s);
+        }
+      } else {
+        return st;
+      }
+      if (e != cudaSuccess) break;
+      e = launch_row_softmax(P->k_rows, P->k_row_ptr, P->H, S, cl, P->ml.as<float>(), P->row_ml.as<float>(), s);
+      if (e != cudaSuccess) break;
+      Geom g2;
+      st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, P->sched.G, P->sched.E, false, 16, g2);
+      if (st != AUTOSAGE_OK) return st;
+      e = launch_spmm(g2, P->k_rows, P->k_row_ptr, P->k_col_idx, S, a.X, ld, a.Y, ld, cl,
+                      P->partial.as<float>(), s);
+      break;
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- estimate
+
+// Estimated time (seconds) of a schedule from row statistics: the larger of
+// the HBM time for the algorithmic bytes (gathers rounded up to 32-byte
+// sectors) and the issue/latency time of all group steps, plus the critical
+// path of the longest work item and a per-launch overhead.
+double estimate(const DeviceInfo &dev, const RowStats &st, autosage_op op, DType dt, int64_t F, int H,
+                const Sched &sc, const Geom &g) {
+  const double n = (double)st.ints[0], nnz = (double)st.ints[1];
+  const int s = dtype_size(dt);
+  const double row_bytes = (double)F * H * s;
+  const double sector = 32.0 * std::ceil(row_bytes / 32.0);
+  double per_edge = 4.0, per_row = 4.0;
+  switch (op) {
+    case AUTOSAGE_OP_SPMM:
+    case AUTOSAGE_OP_SPMM_T: per_edge += 4.0 + sector; per_row += row_bytes; break;
+    case AUTOSAGE_OP_SDDMM: per_edge += 4.0 * H + sector; per_row += row_bytes; break;
+    case AUTOSAGE_OP_ATTN: per_edge += 2.0 * sector; per_row += 2.0 * row_bytes; break;
+    case AUTOSAGE_OP_ATTN_UNFUSED: per_edge += 3.0 * sector + 5.0 * 4.0 * H; per_row += 2.0 * row_bytes; break;
+    case AUTOSAGE_OP_SOFTMAX: per_edge = 3.0 * 4.0 * H; per_row = 4.0; break;
+  }
+  const double bw = dev.bw > 0 ? dev.bw : 6.8e12;
+  const double t_bw = (nnz * per_edge + n * per_row) / bw;
+  // group steps: each edge lane handles U edges per step
+  const int U = g.NV * g.VW <= 8 ? 4 : (g.NV * g.VW <= 16 ? 2 : 1);
+  const double lanes_per_item = (double)g.G * g.E;
+  const double groups = (double)std::max(1, dev.sms) * 48.0 * (32.0 / lanes_per_item);
+  const double lat = 1.2e-6;  // one dependent gather round trip
+  double steps = 0, longest = 0;
+  int64_t split = sc.kind == AUTOSAGE_SCHED_SPLIT ? sc.split : 0;
+  for (int b = 0; b < 32; ++b) {
+    const double cnt = (double)st.ints[8 + b];
+    if (cnt == 0) continue;
+    const double d = b == 0 ? 0.0 : 1.5 * std::pow(2.0, b - 1);
+    double dd = d;
+    double items = 1;
+    if (split > 0 && d > split) {
+      items = std::ceil(d / split);
+      dd = (double)split;
+    }
+    steps += cnt * items * (1.0 + std::ceil(dd / (g.E * U)));
+  }
+  const double maxd = (double)st.ints[2];
+  if (sc.kind == AUTOSAGE_SCHED_MERGEPATH) {
+    const double items = (double)sc.split;
+    steps = (n + nnz) / items * (items / (g.E * U) + 4.0);
+    longest = items / (g.E * U) + 4.0;
+  } else {
+    const double lmax = split > 0 && maxd > split ? (double)split : maxd;
+    longest = 1.0 + std::ceil(lmax / (g.E * U));
+  }
+  const double t_lat = steps * lat / groups;
+  const double t_tail = longest * lat;
+  double launches = 1;
+  if (sc.kind == AUTOSAGE_SCHED_SPLIT && st.ints[6] > 0) launches += (op == AUTOSAGE_OP_SOFTMAX ? 3 : 1);
+  if (sc.kind == AUTOSAGE_SCHED_MERGEPATH) launches += 1;
+  if (op == AUTOSAGE_OP_ATTN_UNFUSED) launches += 2;
+  return std::max(t_bw, t_lat) + t_tail + launches * 3e-6;
+}
+
+// ---------------------------------------------------------------- plan creation
+
+autosage_status make_plan_shell(const autosage_csr *A, autosage_op op, int64_t F, int heads,
+                                autosage_dtype dt, autosage_plan_s **out, cudaStream_t s) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (F < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "F must be >= 1");
+  if (heads < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  if (op < AUTOSAGE_OP_SPMM || op > AUTOSAGE_OP_SOFTMAX) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad op");
+  auto *P = new autosage_plan_s();
+  P->op = op;
+  P->dt = static_cast<DType>(dt);
+  P->F = (op == AUTOSAGE_OP_SOFTMAX) ? 1 : F;
+  P->H = (op == AUTOSAGE_OP_ATTN || op == AUTOSAGE_OP_ATTN_UNFUSED || op == AUTOSAGE_OP_SOFTMAX) ? heads : 1;
+  P->n_rows = A->n_rows;
+  P->n_cols = A->n_cols;
+  P->nnz = A->nnz;
+  P->k_rows = A->n_rows;
+  P->k_row_ptr = A->row_ptr;
+  P->k_col_idx = A->col_idx;
+  P->k_vals = A->vals;
+  if (op == AUTOSAGE_OP_SPMM_T) {
+    cudaError_t e = P->t_row_ptr.alloc(sizeof(int32_t) * (size_t)(A->n_cols + 1));
+    if (e == cudaSuccess) e = P->t_col_idx.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(A->nnz, 1));
+    if (e == cudaSuccess && A->vals) e = P->t_vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(A->nnz, 1));
+    if (e == cudaSuccess)
+      e = csr_transpose(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx, A->vals,
+                        P->t_row_ptr.as<int32_t>(), P->t_col_idx.as<int32_t>(), P->t_vals.as<float>(), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+      delete P;
+      return cuda_fail(e, "building A^T");
+    }
+    P->k_rows = A->n_cols;
+    P->k_row_ptr = P->t_row_ptr.as<int32_t>();
+    P->k_col_idx = P->t_col_idx.as<int32_t>();
+    P->k_vals = A->vals ? P->t_vals.as<float>() : nullptr;
+  }
+  *out = P;
+  return AUTOSAGE_OK;
+}
+
+// Probe buffers shaped like the op's real arguments (never the caller's data).
+struct ProbeBufs {
+  DevBuf X, Y, Y2, Q, K, S;
+  OpArgs a;
+  int64_t out_elems = 0;
+  bool out_is_S = false;
+};
+
+autosage_status make_probe_bufs(const autosage_plan_s *P, ProbeBufs &pb, cudaStream_t s) {
+  const int es = dtype_size(P->dt);
+  const int64_t F = P->F, H = P->H, W = F * H;
+  const int64_t src_rows = (P->op == AUTOSAGE_OP_SPMM_T) ? P->n_rows : P->n_cols;
+  const int64_t dst_rows = P->k_rows;
+  auto alloc_fill = [&](DevBuf &b, int64_t elems, DType dt, uint64_t seed) -> cudaError_t {
+    cudaError_t e = b.alloc((size_t)std::max<int64_t>(elems, 1) * (dt == DType::F32 ? 4 : 2));
+    if (e == cudaSuccess) e = fill_probe(b.p, elems, dt, seed, s);
+    return e;
+  };
+  cudaError_t e = cudaSuccess;
+  switch (P->op) {
+    case AUTOSAGE_OP_SPMM:
+    case AUTOSAGE_OP_SPMM_T:
+      e = alloc_fill(pb.X, src_rows * F, P->dt, 1);
+      if (e == cudaSuccess) e = pb.Y.alloc((size_t)std::max<int64_t>(dst_rows * F, 1) * es);
+      if (e == cudaSuccess) e = pb.Y2.alloc((size_t)std::max<int64_t>(dst_rows * F, 1) * es);
+      pb.a.X = pb.X.p; pb.a.ldx = F; pb.a.Y = pb.Y.p; pb.a.ldy = F;
+      pb.out_elems = dst_rows * F;
+      break;
+    case AUTOSAGE_OP_SDDMM:
+      e = alloc_fill(pb.Q, P->n_rows * F, P->dt, 2);
+      if (e == cudaSuccess) e = alloc_fill(pb.K, P->n_cols * F, P->dt, 3);
+      if (e == cudaSuccess) e = pb.Y.alloc((size_t)std::max<int64_t>(P->nnz, 1) * 4);
+      if (e == cudaSuccess) e = pb.Y2.alloc((size_t)std::max<int64_t>(P->nnz, 1) * 4);
+      pb.a.Q = pb.Q.p; pb.a.ldq = F; pb.a.K = pb.K.p; pb.a.ldk = F; pb.a.S = pb.Y.as<float>();
+      pb.out_elems = P->nnz;
+      pb.out_is_S = true;
+      break;
+    case AUTOSAGE_OP_SOFTMAX:
+      e = alloc_fill(pb.S, P->nnz * H, DType::F32, 4);
+      if (e == cudaSuccess) e = pb.Y.alloc((size_t)std::max<int64_t>(P->nnz * H, 1) * 4);
+      if (e == cudaSuccess) e = pb.Y2.alloc((size_t)std::max<int64_t>(P->nnz * H, 1) * 4);
+      pb.a.S = pb.Y.as<float>();
+      pb.out_elems = P->nnz * H;
+      pb.out_is_S = true;
+      break;
+    case AUTOSAGE_OP_ATTN:
+    case AUTOSAGE_OP_ATTN_UNFUSED:
+      e = alloc_fill(pb.Q, P->n_rows * W, P->dt, 5);
+      if (e == cudaSuccess) e = alloc_fill(pb.K, P->n_cols * W, P->dt, 6);
+      if (e == cudaSuccess) e = alloc_fill(pb.X, P->n_cols * W, P->dt, 7);
+      if (e == cudaSuccess) e = pb.Y.alloc((size_t)std::max<int64_t>(P->n_rows * W, 1) * es);
+      if (e == cudaSuccess) e = pb.Y2.alloc((size_t)std::max<int64_t>(P->n_rows * W, 1) * es);
+      pb.a.Q = pb.Q.p; pb.a.K = pb.K.p; pb.a.X = pb.X.p; pb.a.Y = pb.Y.p;
+      pb.a.alpha = 1.f / std::sqrt((float)F);
+      pb.out_elems = P->n_rows * W;
+      break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "probe buffers");
+  return AUTOSAGE_OK;
+}
+
+// Time one schedule: 1 warm-up, then `reps` timed runs; median in ms.
+autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &ms, cudaStream_t s) {
+  std::vector<float> t;
+  cudaEvent_t e0, e1;
+  CUDA_TRY(cudaEventCreate(&e0));
+  CUDA_TRY(cudaEventCreate(&e1));
+  OpArgs a = pb.a;
+  if (P->op == AUTOSAGE_OP_ATTN_UNFUSED) a.S = P->scores.as<float>();
+  autosage_status st = AUTOSAGE_OK;
+  for (int r = 0; r <= reps && st == AUTOSAGE_OK; ++r) {
+    if (P->op == AUTOSAGE_OP_SOFTMAX)
+      cudaMemcpyAsync(pb.Y.p, pb.S.p, (size_t)pb.out_elems * 4, cudaMemcpyDeviceToDevice, s);
+    cudaEventRecord(e0, s);
+    st = run_op(P, P->op, a, s);
+    cudaEventRecord(e1, s);
+    cudaError_t e = cudaEventSynchronize(e1);
+    if (e != cudaSuccess) st = cuda_fail(e, "probe");
+    float x = 0;
+    cudaEventElapsedTime(&x, e0, e1);
+    if (r > 0) t.push_back(x);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != AUTOSAGE_OK) return st;
+  std::sort(t.begin(), t.end());
+  ms = t[t.size() / 2];
+  return AUTOSAGE_OK;
+}
+
+bool same_sched(const Sched &a, const Sched &b) {
+  return a.kind == b.kind && a.G == b.G && a.E == b.E && a.split == b.split;
+}
+
+struct Candidate {
+  Sched sc;
+  double est;
+};
+
+// Candidate schedules for the op and its statistics.
+std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *P, const RowStats &st) {
+  std::vector<Candidate> out;
+  const OpShape sh = op_shape(P->op, P->F, P->H);
+  // lanes across features from the width (what choose_geom would pick)
+  const int s = dtype_size(P->dt);
+  const int64_t Fb = P->F * sh.H * s;
+  int vb = 16;
+  while (vb > s && (P->F * s) % vb) vb >>= 1;
+  const int64_t nfrag = std::max<int64_t>(1, (P->F * sh.H * s) / vb);
+  (void)Fb;
+  std::vector<int> Gs;
+  const int G0 = std::min(32, pow2ceil(nfrag));
+  Gs.push_back(G0);
+  if (G0 > 1 && P->op != AUTOSAGE_OP_SOFTMAX) Gs.push_back(G0 / 2);
+  const int64_t maxd = st.ints[2];
+  for (int G : Gs) {
+    if (P->op == AUTOSAGE_OP_SOFTMAX && G != G0) continue;
+    for (int E = 1; G * E <= 32; E <<= 1) {
+      if (P->op == AUTOSAGE_OP_SOFTMAX && E > 1) break;
+      Geom g{};
+      g.dt = P->dt; g.H = sh.H; g.D = sh.D; g.VW = vb / s; g.nfrag = (int)nfrag; g.G = G; g.E = E;
+      g.NV = pow2ceil((nfrag + G - 1) / G);
+      if (g.NV > sh.nv_max) continue;
+      Sched rg{AUTOSAGE_SCHED_ROWGROUP, G, E, 0};
+      out.push_back({rg, estimate(dev, st, P->op, P->dt, P->F, sh.H, rg, g)});
+      for (int split : {128, 512, 2048, 8192}) {
+        if (maxd <= split) continue;
+        Sched sp{AUTOSAGE_SCHED_SPLIT, G, E, split};
+        out.push_back({sp, estimate(dev, st, P->op, P->dt, P->F, sh.H, sp, g)});
+      }
+      if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && G * E == 32) {
+        for (int items : {256, 1024}) {
+          Sched mp{AUTOSAGE_SCHED_MERGEPATH, G, E, items};
+          out.push_back({mp, estimate(dev, st, P->op, P->dt, P->F, sh.H, mp, g)});
+        }
+      }
+    }
+  }
+  std::stable_sort(out.begin(), out.end(), [](const Candidate &a, const Candidate &b) { return a.est < b.est; });
+  return out;
+}
+
+void log_line(const char *fmt, ...) {
+  const char *path = getenv("AUTOSAGE_LOG");
+  if (!path || !*path) return;
+  FILE *f = fopen(path, "a");
+  if (!f) return;
+  va_list ap;
+  va_start(ap, fmt);
+  vfprintf(f, fmt, ap);
+  va_end(ap);
+  fputc('\n', f);
+  fclose(f);
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char *autosage_version(void) { return "autosage-gb300 0.1"; }
+
+const char *autosage_status_string(autosage_status s) {
+  switch (s) {
+    case AUTOSAGE_OK: return "ok";
+    case AUTOSAGE_ERR_INVALID_ARG: return "invalid argument";
+    case AUTOSAGE_ERR_INVALID_CSR: return "invalid CSR structure";
+    case AUTOSAGE_ERR_UNSUPPORTED: return "unsupported shape";
+    case AUTOSAGE_ERR_CUDA: return "CUDA error";
+    case AUTOSAGE_ERR_CACHE_IO: return "cache file I/O error";
+    case AUTOSAGE_ERR_CACHE_FORMAT: return "cache file format error";
+    case AUTOSAGE_ERR_PROBE: return "every probed schedule failed";
+    case AUTOSAGE_ERR_PLAN_MISMATCH: return "plan does not match the call";
+  }
+  return "unknown status";
+}
+
+const char *autosage_last_error(void) { return g_last_error.c_str(); }
+
+autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op op, int64_t F, int heads,
+                                            autosage_dtype dt, const autosage_schedule *sched,
+                                            autosage_plan_t *out, void *stream) {
+  if (!out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!sched) return fail(AUTOSAGE_ERR_INVALID_ARG, "sched is NULL");
+  if (sched->kind < AUTOSAGE_SCHED_ROWGROUP || sched->kind > AUTOSAGE_SCHED_MERGEPATH)
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "bad schedule kind");
+  if ((sched->lanes_f && !is_pow2(sched->lanes_f)) || (sched->lanes_e && !is_pow2(sched->lanes_e)) ||
+      sched->lanes_f > 32 || sched->lanes_e > 32 || sched->lanes_f * std::max(1, sched->lanes_e) > 32)
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "lanes must be powers of two with lanes_f * lanes_e <= 32");
+  if (sched->split < 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "negative split");
+  cudaStream_t s = as_stream(stream);
+  autosage_plan_s *P = nullptr;
+  autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
+  if (st != AUTOSAGE_OK) return st;
+  P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split};
+  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT && P->sched.split == 0) P->sched.split = 1024;
+  if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH && P->sched.split == 0) P->sched.split = 512;
+  if (P->sched.kind == AUTOSAGE_SCHED_ROWGROUP) P->sched.split = 0;
+  st = build_workspace(P, s);
+  if (st != AUTOSAGE_OK) {
+    delete P;
+    return st;
+  }
+  *out = P;
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, int heads,
+                              autosage_dtype dt, unsigned flags, autosage_plan_t *out, void *stream) {
+  if (!out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  cudaStream_t s = as_stream(stream);
+  autosage_plan_s *P = nullptr;
+  autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
+  if (st != AUTOSAGE_OK) return st;
+  const DeviceInfo dev = device_info();
+  // structure statistics and fingerprint of the CSR the kernels walk
+  RowStats rs;
+  st = gpu_row_stats(P->k_rows, P->k_row_ptr, 1024, rs, s);
+  if (st != AUTOSAGE_OK) {
+    delete P;
+    return st;
+  }
+  uint64_t fp = 0;
+  {
+    autosage_csr K{P->k_rows, (op == AUTOSAGE_OP_SPMM_T) ? A->n_rows : A->n_cols, P->nnz,
+                   P->k_row_ptr, P->k_col_idx, P->k_vals};
+    st = autosage_fingerprint(&K, &fp, stream);
+    if (st != AUTOSAGE_OK) {
+      delete P;
+      return st;
+    }
+  }
+  const std::string key = cache_key(dev, op, P->dt, P->F, P->H, A->n_rows, A->n_cols, A->nnz, fp);
+  const bool use_cache = !(flags & AUTOSAGE_PLAN_NO_CACHE);
+  if (use_cache) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    auto it = g_cache.find(key);
+    if (it != g_cache.end()) {
+      P->sched = it->second.sched;
+      P->probe_ms = it->second.probe_ms;
+      P->from_cache = true;
+    }
+  }
+  if (P->from_cache) {
+    st = build_workspace(P, s);
+    if (st == AUTOSAGE_OK) {
+      log_line("plan key=%s cache-hit %s G=%d E=%d split=%d", key.c_str(), sched_name(P->sched.kind),
+               P->sched.G, P->sched.E, P->sched.split);
+      *out = P;
+      return AUTOSAGE_OK;
+    }
+    // a stale entry falls through to a fresh choice
+    P->from_cache = false;
+  }
+  std::vector<Candidate> cands = candidates(dev, P, rs);
+  const bool probe = (flags & AUTOSAGE_PLAN_PROBE) != 0;
+  const bool verify = (flags & AUTOSAGE_PLAN_VERIFY) != 0;
+  Sched best = default_sched();
+  double best_ms = -1, best_est = -1;
+  autosage_status result = AUTOSAGE_OK;
+  if (!probe) {
+    if (!cands.empty()) {
+      best = cands[0].sc;
+      best_est = cands[0].est;
+    }
+  } else {
+    // top-3 by estimate, plus the guardrail default
+    std::vector<Candidate> top;
+    for (const Candidate &c : cands) {
+      if ((int)top.size() >= 3) break;
+      top.push_back(c);
+    }
+    top.push_back({default_sched(), -1});
+    ProbeBufs pb;
+    st = make_probe_bufs(P, pb, s);
+    if (st != AUTOSAGE_OK) {
+      delete P;
+      return st;
+    }
+    // the guardrail's output for the spot check
+    bool have_ref = false;
+    if (verify) {
+      P->sched = default_sched();
+      if (build_workspace(P, s) == AUTOSAGE_OK) {
+        OpArgs a = pb.a;
+        if (op == AUTOSAGE_OP_ATTN_UNFUSED) a.S = P->scores.as<float>();
+        if (op == AUTOSAGE_OP_SOFTMAX)
+          cudaMemcpyAsync(pb.Y.p, pb.S.p, (size_t)pb.out_elems * 4, cudaMemcpyDeviceToDevice, s);
+        if (run_op(P, op, a, s) == AUTOSAGE_OK && cudaStreamSynchronize(s) == cudaSuccess) {
+          const size_t bytes = (size_t)pb.out_elems * (pb.out_is_S ? 4 : dtype_size(P->dt));
+          have_ref = cudaMemcpyAsync(pb.Y2.p, pb.Y.p, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+        }
+      }
+    }
+    int ok_count = 0;
+    for (const Candidate &c : top) {
+      P->sched = c.sc;
+      if (build_workspace(P, s) != AUTOSAGE_OK) continue;
+      double ms = 0;
+      if (probe_time(P, pb, 5, ms, s) != AUTOSAGE_OK) continue;
+      if (verify && have_ref && !same_sched(c.sc, default_sched())) {
+        unsigned long long *cnt = nullptr, h = 1;
+        if (cudaMallocAsync(&cnt, sizeof *cnt, s) == cudaSuccess) {
+          const DType cdt = pb.out_is_S ? DType::F32 : P->dt;
+          const float rtol = cdt == DType::F32 ? 1e-4f : 2e-2f;
+          launch_compare(pb.Y.p, pb.Y2.p, pb.out_elems, cdt, rtol, rtol, cnt, s);
+          cudaMemcpyAsync(&h, cnt, sizeof h, cudaMemcpyDeviceToHost, s);
+          cudaFreeAsync(cnt, s);
+          cudaStreamSynchronize(s);
+        }
+        if (h != 0) {
+          log_line("plan key=%s reject %s G=%d E=%d split=%d mismatches=%llu", key.c_str(),
+                   sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, h);
+          continue;
+        }
+      }
+      ++ok_count;
+      log_line("plan key=%s probe %s G=%d E=%d split=%d est_ms=%.4f probe_ms=%.4f", key.c_str(),
+               sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, c.est * 1e3, ms);
+      if (best_ms < 0 || ms < best_ms) {
+        best_ms = ms;
+        best = c.sc;
+        best_est = c.est;
+      }
+    }
+    cudaGetLastError();  // a failed candidate must not poison later calls
+    if (ok_count == 0) {
+      best = default_sched();
+      result = fail(AUTOSAGE_ERR_PROBE, "every probed schedule failed; using the default");
+    }
+  }
+  P->sched = best;
+  P->probe_ms = best_ms;
+  P->est_ms = best_est * 1e3;
+  st = build_workspace(P, s);
+  if (st != AUTOSAGE_OK && !same_sched(best, default_sched())) {
+    P->sched = default_sched();
+    st = build_workspace(P, s);
+  }
+  if (st != AUTOSAGE_OK) {
+    delete P;
+    return st;
+  }
+  if (use_cache && (probe || !cands.empty())) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    g_cache[key] = CacheEntry{P->sched, P->probe_ms};
+  }
+  log_line("plan key=%s choose %s G=%d E=%d split=%d est_ms=%.4f probe_ms=%.4f", key.c_str(),
+           sched_name(P->sched.kind), P->sched.G, P->sched.E, P->sched.split, P->est_ms, P->probe_ms);
+  *out = P;
+  return result;
+}
+
+autosage_status autosage_plan_destroy(autosage_plan_t plan) {
+  if (!plan) return AUTOSAGE_OK;
+  cudaDeviceSynchronize();
+  delete plan;
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_plan_describe(autosage_plan_t P, char *buf, size_t len) {
+  if (!P || !buf || len == 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad describe arguments");
+  snprintf(buf, len, "op=%d sched=%s G=%d E=%d split=%d chunks=%d long_rows=%d mp_warps=%" PRId64
+           " probe_ms=%.4f est_ms=%.4f cache=%d",
+           (int)P->op, sched_name(P->sched.kind), P->sched.G, P->sched.E, P->sched.split, P->cl.n_chunks,
+           P->cl.n_long, P->mp_warps, P->probe_ms, P->est_ms, P->from_cache ? 1 : 0);
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_plan_schedule(autosage_plan_t P, autosage_schedule *sched, double *probe_ms) {
+  if (!P) return fail(AUTOSAGE_ERR_INVALID_ARG, "plan is NULL");
+  if (sched) {
+    sched->kind = P->sched.kind;
+    sched->lanes_f = P->sched.G;
+    sched->lanes_e = P->sched.E;
+    sched->split = P->sched.split;
+  }
+  if (probe_ms) *probe_ms = P->probe_ms;
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- ops
+
+static autosage_status plan_matches(const autosage_plan_s *P, const autosage_csr *A, autosage_op op,
+                                    int64_t F, int H, autosage_dtype dt) {
+  if (P->op != op) return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for op %d, called as op %d", (int)P->op, (int)op);
+  if (P->n_rows != A->n_rows || P->n_cols != A->n_cols || P->nnz != A->nnz)
+    return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for another graph");
+  if (P->F != F || P->H != H || (int)P->dt != (int)dt)
+    return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for another width, head count or dtype");
+  return AUTOSAGE_OK;
+}
+
+// A transient plan with the default schedule and no workspace.
+static autosage_plan_s transient(const autosage_csr *A, autosage_op op, int64_t F, int H, autosage_dtype dt) {
+  autosage_plan_s P;
+  P.op = op;
+  P.dt = static_cast<DType>(dt);
+  P.F = F;
+  P.H = H;
+  P.n_rows = A->n_rows;
+  P.n_cols = A->n_cols;
+  P.nnz = A->nnz;
+  P.k_rows = A->n_rows;
+  P.k_row_ptr = A->row_ptr;
+  P.k_col_idx = A->col_idx;
+  P.k_vals = A->vals;
+  P.sched = default_sched();
+  return P;
+}
+
+static autosage_status check_mat(const void *p, int64_t ld, int64_t width, int64_t rows, const char *name) {
+  if (rows > 0 && !p) return fail(AUTOSAGE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (ld < width) return fail(AUTOSAGE_ERR_INVALID_ARG, "%s: leading dimension < width", name);
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_spmm(const autosage_csr *A, const void *X, int64_t ldx, void *Y, int64_t ldy,
+                              int64_t F, autosage_dtype dt, int transpose, autosage_plan_t plan,
+                              void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (F < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "F must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  const int64_t out_rows = transpose ? A->n_cols : A->n_rows;
+  const int64_t in_rows = transpose ? A->n_rows : A->n_cols;
+  if ((st = check_mat(X, ldx, F, in_rows, "X")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(Y, ldy, F, out_rows, "Y")) != AUTOSAGE_OK) return st;
+  if (out_rows == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.X = X; a.ldx = ldx; a.Y = Y; a.ldy = ldy;
+  const autosage_op op = transpose ? AUTOSAGE_OP_SPMM_T : AUTOSAGE_OP_SPMM;
+  if (plan) {
+    if ((st = plan_matches(plan, A, op, F, 1, dt)) != AUTOSAGE_OK) return st;
+    return run_op(plan, op, a, as_stream(stream));
+  }
+  if (transpose) return fail(AUTOSAGE_ERR_INVALID_ARG, "transpose needs a plan built for AUTOSAGE_OP_SPMM_T");
+  autosage_plan_s P = transient(A, op, F, 1, dt);
+  return run_op(&P, op, a, as_stream(stream));
+}
+
+autosage_status autosage_sddmm(const autosage_csr *A, const void *Q, int64_t ldq, const void *K, int64_t ldk,
+                               int64_t F, autosage_dtype dt, float alpha, float *out, autosage_plan_t plan,
+                               void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (F < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "F must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  if ((st = check_mat(Q, ldq, F, A->n_rows, "Q")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(K, ldk, F, A->n_cols, "K")) != AUTOSAGE_OK) return st;
+  if (A->nnz > 0 && !out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
+  if (A->nnz == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.Q = Q; a.ldq = ldq; a.K = K; a.ldk = ldk; a.alpha = alpha; a.S = out;
+  if (plan) {
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_SDDMM, F, 1, dt)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_SDDMM, a, as_stream(stream));
+  }
+  autosage_plan_s P = transient(A, AUTOSAGE_OP_SDDMM, F, 1, dt);
+  return run_op(&P, AUTOSAGE_OP_SDDMM, a, as_stream(stream));
+}
+
+autosage_status autosage_row_softmax(const autosage_csr *A, float *scores, int heads, autosage_plan_t plan,
+                                     void *stream) {
+  autosage_status st = check_csr(A, false);
+  if (st != AUTOSAGE_OK) return st;
+  if (heads < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads must be >= 1");
+  if (A->nnz > 0 && !scores) return fail(AUTOSAGE_ERR_INVALID_ARG, "scores is NULL");
+  if (A->nnz == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.S = scores;
+  if (plan) {
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_SOFTMAX, 1, heads, AUTOSAGE_F32)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_SOFTMAX, a, as_stream(stream));
+  }
+  autosage_plan_s P = transient(A, AUTOSAGE_OP_SOFTMAX, 1, heads, AUTOSAGE_F32);
+  return run_op(&P, AUTOSAGE_OP_SOFTMAX, a, as_stream(stream));
+}
+
+autosage_status autosage_csr_attention(const autosage_csr *A, const void *Q, const void *K, const void *V,
+                                       int heads, int64_t D, autosage_dtype dt, float scale, void *out,
+                                       int fused, autosage_plan_t plan, void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (heads < 1 || D < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads and D must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  const int64_t W = (int64_t)heads * D;
+  if ((st = check_mat(Q, W, W, A->n_rows, "Q")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(K, W, W, A->n_cols, "K")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(V, W, W, A->n_cols, "V")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(out, W, W, A->n_rows, "out")) != AUTOSAGE_OK) return st;
+  if (A->n_rows == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.Q = Q; a.K = K; a.X = V; a.Y = out; a.alpha = scale;
+  cudaStream_t s = as_stream(stream);
+  const autosage_op op = fused ? AUTOSAGE_OP_ATTN : AUTOSAGE_OP_ATTN_UNFUSED;
+  if (plan) {
+    if ((st = plan_matches(plan, A, op, D, heads, dt)) != AUTOSAGE_OK) return st;
+    if (!fused) a.S = plan->scores.as<float>();
+    return run_op(plan, op, a, s);
+  }
+  autosage_plan_s P = transient(A, op, D, heads, dt);
+  if (fused) return run_op(&P, op, a, s);
+  float *S = nullptr;
+  cudaError_t e = cudaMallocAsync(&S, sizeof(float) * (size_t)std::max<int64_t>(A->nnz * heads, 1), s);
+  if (e != cudaSuccess) return cuda_fail(e, "score buffer");
+  a.S = S;
+  st = run_op(&P, op, a, s);
+  cudaFreeAsync(S, s);
+  return st;
+}
+
+autosage_status autosage_edge_softmax_aggregate(const autosage_csr *A, const float *scores, const void *V,
+                                                int heads, int64_t D, autosage_dtype dt, void *out,
+                                                autosage_plan_t plan, void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (heads < 1 || D < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads and D must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  const int64_t W = (int64_t)heads * D;
+  if (A->nnz > 0 && !scores) return fail(AUTOSAGE_ERR_INVALID_ARG, "scores is NULL");
+  if ((st = check_mat(V, W, W, A->n_cols, "V")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(out, W, W, A->n_rows, "out")) != AUTOSAGE_OK) return st;
+  if (A->n_rows == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.X = V; a.Y = out; a.given = scores;
+  if (plan) {
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_ATTN, D, heads, dt)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_ATTN, a, as_stream(stream));
+  }
+  autosage_plan_s P = transient(A, AUTOSAGE_OP_ATTN, D, heads, dt);
+  return run_op(&P, AUTOSAGE_OP_ATTN, a, as_stream(stream));
+}
+
+// ---------------------------------------------------------------- utilities
+
+autosage_status autosage_row_stats(const autosage_csr *A, int64_t long_threshold, int64_t *ints, double *reals,
+                                   void *stream) {
+  autosage_status st = check_csr(A, false);
+  if (st != AUTOSAGE_OK) return st;
+  if (!ints || !reals) return fail(AUTOSAGE_ERR_INVALID_ARG, "output arrays are NULL");
+  RowStats rs;
+  st = gpu_row_stats(A->n_rows, A->row_ptr, long_threshold, rs, as_stream(stream));
+  if (st != AUTOSAGE_OK) return st;
+  for (int i = 0; i < 40; ++i) ints[i] = rs.ints[i];
+  reals[0] = rs.mean;
+  reals[1] = rs.cv;
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_fingerprint(const autosage_csr *A, uint64_t *out, void *stream) {
+  autosage_status st = check_csr(A, false);
+  if (st != AUTOSAGE_OK) return st;
+  if (!out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
+  cudaStream_t s = as_stream(stream);
+  unsigned long long *d = nullptr, h = 0;
+  CUDA_TRY(cudaMallocAsync(&d, sizeof h, s));
+  cudaError_t e = launch_fingerprint(A->n_rows, A->nnz, A->row_ptr, A->col_idx, d, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof h, cudaMemcpyDeviceToHost, s);
+  cudaFreeAsync(d, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "fingerprint");
+  // the seed term mix(n_rows) is added on the host
+  uint64_t z = (uint64_t)A->n_rows;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  z ^= z >> 31;
+  *out = h + z;
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_validate_csr(const autosage_csr *A, void *stream) {
+  if (!A || !A->row_ptr || A->n_rows < 0 || A->nnz < 0 || (A->nnz > 0 && !A->col_idx))
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "bad CSR descriptor");
+  cudaStream_t s = as_stream(stream);
+  int *d = nullptr, h = 0;
+  CUDA_TRY(cudaMallocAsync(&d, sizeof h, s));
+  cudaError_t e = launch_validate(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx, d, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof h, cudaMemcpyDeviceToHost, s);
+  cudaFreeAsync(d, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "validate");
+  if (h) return fail(AUTOSAGE_ERR_INVALID_CSR, "invalid CSR (flags 0x%x: 1 row_ptr[0]!=0, 2 decreasing row_ptr, "
+                     "4 row_ptr[n]!=nnz, 8 col_idx out of range)", h);
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_csr_transpose(const autosage_csr *A, int32_t *row_ptr_t, int32_t *col_idx_t,
+                                       float *vals_t, void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (!row_ptr_t || (A->nnz > 0 && !col_idx_t)) return fail(AUTOSAGE_ERR_INVALID_ARG, "output is NULL");
+  cudaError_t e = csr_transpose(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx,
+                                vals_t ? A->vals : nullptr, row_ptr_t, col_idx_t, vals_t,
+                                as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "transpose");
+  return AUTOSAGE_OK;
+}
+
+// ---------------------------------------------------------------- cache I/O
+
+autosage_status autosage_cache_clear(void) {
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  g_cache.clear();
+  return AUTOSAGE_OK;
+}
+
+int64_t autosage_cache_size(void) {
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  return (int64_t)g_cache.size();
+}
+
+autosage_status autosage_cache_save(const char *path) {
+  if (!path) return fail(AUTOSAGE_ERR_INVALID_ARG, "path is NULL");
+  std::string tmp = std::string(path) + ".tmp";
+  FILE *f = fopen(tmp.c_str(), "w");
+  if (!f) return fail(AUTOSAGE_ERR_CACHE_IO, "cannot write %s", tmp.c_str());
+  {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    fprintf(f, "%s\n", kCacheHeader);
+    for (const auto &kv : g_cache)
+      fprintf(f, "%s\t%s %d %d %d %.6f\n", kv.first.c_str(), sched_name(kv.second.sched.kind),
+              kv.second.sched.G, kv.second.sched.E, kv.second.sched.split, kv.second.probe_ms);
+  }
+  const bool ok = fflush(f) == 0;
+  fclose(f);
+  if (!ok || rename(tmp.c_str(), path) != 0) return fail(AUTOSAGE_ERR_CACHE_IO, "cannot replace %s", path);
+  return AUTOSAGE_OK;
+}
+
+autosage_status autosage_cache_load(const char *path) {
+  if (!path) return fail(AUTOSAGE_ERR_INVALID_ARG, "path is NULL");
+  std::ifstream in(path);
+  if (!in) return fail(AUTOSAGE_ERR_CACHE_IO, "cannot read %s", path);
+  std::string line;
+  if (!std::getline(in, line) || line != kCacheHeader)
+    return fail(AUTOSAGE_ERR_CACHE_FORMAT, "%s: missing or wrong header", path);
+  int bad = 0, lineno = 1;
+  std::map<std::string, CacheEntry> got;
+  while (std::getline(in, line)) {
+    ++lineno;
+    if (line.empty() || line[0] == '#') continue;
+    const size_t tab = line.find('\t');
+    if (tab == std::string::npos || tab == 0) {
+      ++bad;
+      continue;
+    }
+    std::istringstream vs(line.substr(tab + 1));
+    std::string kind;
+    CacheEntry e;
+    if (!(vs >> kind >> e.sched.G >> e.sched.E >> e.sched.split >> e.probe_ms)) {
+      ++bad;
+      continue;
+    }
+    std::string rest;
+    if (vs >> rest) {
+      ++bad;
+      continue;
+    }
+    if (kind == "rowgroup") e.sched.kind = AUTOSAGE_SCHED_ROWGROUP;
+    else if (kind == "split") e.sched.kind = AUTOSAGE_SCHED_SPLIT;
+    else if (kind == "mergepath") e.sched.kind = AUTOSAGE_SCHED_MERGEPATH;
+    else {
+      ++bad;
+      continue;
+    }
+    const Sched &s = e.sched;
+    const bool lanes_ok = (s.G == 0 || (is_pow2(s.G) && s.G <= 32)) && (s.E == 0 || (is_pow2(s.E) && s.E <= 32)) &&
+                          std::max(1, s.G) * std::max(1, s.E) <= 32;
+    const bool split_ok = s.kind == AUTOSAGE_SCHED_ROWGROUP ? s.split == 0 : s.split > 0;
+    if (!lanes_ok || !split_ok) {
+      ++bad;
+      continue;
+    }
+    got[line.substr(0, tab)] = e;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    for (auto &kv : got) g_cache[kv.first] = kv.second;
+  }
+  if (bad) return fail(AUTOSAGE_ERR_CACHE_FORMAT, "%s: %d bad line(s) skipped", path, bad);
+  return AUTOSAGE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,391 @@
+// CSR SpMM kernels: Y = A X (AutoSAGE, "Input-Aware CUDA Scheduling for
+// Sparse GNN Aggregation (SpMM/SDDMM) and CSR Attention", Abstract: "CSR
+// SpMM"), with per-head edge weights for the aggregation step of CSR
+// attention (Abstract: "SDDMM -> row-softmax -> SpMM").
+//
+// The work is a gather: every edge reads one source row of X. Kernels are
+// HBM-bound; they use no tensor cores. Three schedules:
+//  * row groups: G feature lanes x E edge lanes per row (rows of degree
+//    <= split), E partial sums combined by shuffles in a fixed order;
+//  * split: rows longer than `split` edges are cut into chunks that write
+//    fp32 partials; a fix-up adds each row's chunks in chunk order;
+//  * merge path: each warp takes an equal share of (rows + edges); rows cut
+//    at warp boundaries leave carry-outs that a fix-up adds in warp order.
+// No floating-point atomics anywhere: repeat runs give identical bits.
+#include "internal.h"
+
+namespace autosage {
+
+namespace {
+
+template <int NV, int VW>
+__device__ __forceinline__ void zero(float (&acc)[NV][VW]) {
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int v = 0; v < VW; ++v) acc[k][v] = 0.f;
+}
+
+// Accumulate edges p = p0, p0 + E, ... < pe into acc (per lane fragments).
+template <typename T, int VW, int NV, int U>
+__device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx,
+                                             const float *__restrict__ vals, int H, int es,
+                                             const int (&head)[NV], const T *__restrict__ X,
+                                             int64_t ldx, int nfrag, int g, int G, int E, int p0,
+                                             int pe, float (&acc)[NV][VW]) {
+  int p = p0;
+  if constexpr (U > 1) {
+    for (; p + (U - 1) * E < pe; p += U * E) {
+      int c[U];
+      float w[U][NV];
+#pragma unroll
+      for (int u = 0; u < U; ++u) c[u] = ld_stream_i32(col_idx + p + u * E);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (vals == nullptr) {
+#pragma unroll
+          for (int k = 0; k < NV; ++k) w[u][k] = 1.f;
+        } else if (H == 1) {
+          const float x = ld_stream_f32(vals + (int64_t)(p + u * E) * es);
+#pragma unroll
+          for (int k = 0; k < NV; ++k) w[u][k] = x;
+        } else {
+#pragma unroll
+          for (int k = 0; k < NV; ++k) w[u][k] = __ldg(vals + (int64_t)(p + u * E) * es + head[k]);
+        }
+      }
+      Frag<T, VW> f[U][NV];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (g + k * G < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)(g + k * G) * VW);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (g + k * G < nfrag)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[u][k], f[u][k].get(v), acc[k][v]);
+    }
+  }
+  for (; p < pe; p += E) {
+    const int c = ld_stream_i32(col_idx + p);
+    float w[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      w[k] = vals == nullptr ? 1.f
+             : H == 1        ? __ldg(vals + (int64_t)p * es)
+                             : __ldg(vals + (int64_t)p * es + head[k]);
+    Frag<T, VW> f[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (g + k * G < nfrag) f[k].load(X + (int64_t)c * ldx + (int64_t)(g + k * G) * VW);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (g + k * G < nfrag)
+#pragma unroll
+        for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[k], f[k].get(v), acc[k][v]);
+  }
+}
+
+// Sum the E edge-lane partials of a group (xor butterfly, fixed order).
+template <int NV, int VW>
+__device__ __forceinline__ void reduce_edge_lanes(float (&acc)[NV][VW], unsigned mask, int G, int GE) {
+  for (int off = G; off < GE; off <<= 1) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int v = 0; v < VW; ++v) acc[k][v] += __shfl_xor_sync(mask, acc[k][v], off);
+  }
+}
+
+template <int NV, int VW> constexpr int unroll_for() {
+  return NV * VW <= 8 ? 4 : (NV * VW <= 16 ? 2 : 1);
+}
+
+template <typename T, int VW, int NV>
+__global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
+    int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
+    const float *__restrict__ vals, int H, int es, int cph, const T *__restrict__ X, int64_t ldx,
+    T *__restrict__ Y, int64_t ldy, int nfrag, int G, int E, ChunkList cl, int64_t chunk_blocks,
+    float *__restrict__ partial) {
+  const Lanes L(G, E);
+  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  int head[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = L.g + k * G;
+    head[k] = (H > 1 && c < nfrag) ? c / cph : 0;
+  }
+  float acc[NV][VW];
+  zero(acc);
+  gather_edges<T, VW, NV, unroll_for<NV, VW>()>(col_idx, vals, H, es, head, X, ldx, nfrag, L.g, G, E,
+                                                 it.b + L.e, it.e, acc);
+  reduce_edge_lanes(acc, L.group_mask, G, L.GE);
+  if (!it.active || L.e != 0) return;
+  if (it.chunk < 0) {
+    T *y = Y + it.row * ldy;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (L.g + k * G < nfrag) store_frag<T, VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+  } else {
+    float *y = partial + (int64_t)it.chunk * nfrag * VW;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (L.g + k * G < nfrag) store_partial<VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+  }
+}
+
+// One warp per cut row: add its chunk partials in chunk order.
+template <typename T, int VW>
+__global__ void __launch_bounds__(kBlock) spmm_fixup_kernel(ChunkList cl, int nfrag,
+                                                            const float *__restrict__ partial,
+                                                            T *__restrict__ Y, int64_t ldy) {
+  const int64_t j = (int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5);
+  if (j >= cl.n_long) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = cl.long_rows[j];
+  const int c0 = cl.long_ptr[j], c1 = cl.long_ptr[j + 1];
+  const int64_t F = (int64_t)nfrag * VW;
+  for (int f = lane; f < nfrag; f += 32) {
+    float acc[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+    for (int c = c0; c < c1; ++c) {
+      const float *src = partial + (int64_t)c * F + (int64_t)f * VW;
+#pragma unroll
+      for (int v = 0; v < VW; ++v) acc[v] += __ldcg(src + v);
+    }
+    store_frag<T, VW>(Y + row * ldy + (int64_t)f * VW, acc);
+  }
+}
+
+// ---------------------------------------------------------------- merge path
+
+// Diagonal d of the merge of row ends (row_ptr[1..n]) with edge indices:
+// returns (rows consumed, edges consumed), row ends taken first on ties.
+__device__ __forceinline__ int2 merge_path_search(int64_t d, int64_t n_rows, int64_t nnz,
+                                                  const int32_t *__restrict__ row_ptr) {
+  int64_t lo = d - nnz > 0 ? d - nnz : 0;
+  int64_t hi = d < n_rows ? d : n_rows;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if ((int64_t)row_ptr[mid + 1] <= d - mid - 1)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return make_int2(static_cast<int>(lo), static_cast<int>(d - lo));
+}
+
+__global__ void mergepath_partition_kernel(int64_t n_rows, int64_t nnz,
+                                           const int32_t *__restrict__ row_ptr, int64_t items,
+                                           int64_t n_warps, int2 *__restrict__ part) {
+  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (w > n_warps) return;
+  int64_t d = w * items;
+  if (d > n_rows + nnz) d = n_rows + nnz;
+  part[w] = merge_path_search(d, n_rows, nnz, row_ptr);
+}
+
+template <typename T, int VW, int NV>
+__global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
+    int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
+    const float *__restrict__ vals, const T *__restrict__ X, int64_t ldx, T *__restrict__ Y,
+    int64_t ldy, int nfrag, int G, int E, const int2 *__restrict__ part, int64_t n_warps,
+    float *__restrict__ carry_val, int32_t *__restrict__ carry_row) {
+  const int64_t w = (int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5);
+  if (w >= n_warps) return;  // whole warps leave together
+  const Lanes L(G, E);       // G * E == 32: one group per warp
+  const int2 s0 = part[w], s1 = part[w + 1];
+  const int head[NV] = {};
+  constexpr int U = unroll_for<NV, VW>();
+  for (int i = s0.x; i < s1.x; ++i) {
+    const int b = max(row_ptr[i], s0.y), e = row_ptr[i + 1];
+    float acc[NV][VW];
+    zero(acc);
+    gather_edges<T, VW, NV, U>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, e, acc);
+    reduce_edge_lanes(acc, FULL, G, 32);
+    if (L.e == 0) {
+      T *y = Y + (int64_t)i * ldy;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (L.g + k * G < nfrag) store_frag<T, VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+    }
+  }
+  // the row left unfinished at the warp's end becomes a carry-out
+  int crow = -1;
+  if (s1.x < n_rows) {
+    const int b = max(row_ptr[s1.x], s0.y);
+    if (s1.y > b) {
+      crow = s1.x;
+      float acc[NV][VW];
+      zero(acc);
+      gather_edges<T, VW, NV, U>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, s1.y, acc);
+      reduce_edge_lanes(acc, FULL, G, 32);
+      if (L.e == 0) {
+        float *cv = carry_val + w * (int64_t)nfrag * VW;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (L.g + k * G < nfrag) store_partial<VW>(cv + (int64_t)(L.g + k * G) * VW, acc[k]);
+      }
+    }
+  }
+  if (L.lane == 0) carry_row[w] = crow;
+}
+
+// The first warp carrying a row adds every carry of that row (in warp order)
+// to the value the row's finishing warp wrote.
+template <typename T, int VW>
+__global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
+    int64_t n_warps, int nfrag, const float *__restrict__ carry_val,
+    const int32_t *__restrict__ carry_row, T *__restrict__ Y, int64_t ldy) {
+  const int64_t w = (int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5);
+  if (w >= n_warps) return;
+  const int r = carry_row[w];
+  if (r < 0 || (w > 0 && carry_row[w - 1] == r)) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t F = (int64_t)nfrag * VW;
+  for (int f = lane; f < nfrag; f += 32) {
+    float acc[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+    for (int64_t q = w; q < n_warps && carry_row[q] == r; ++q) {
+      const float *src = carry_val + q * F + (int64_t)f * VW;
+#pragma unroll
+      for (int v = 0; v < VW; ++v) acc[v] += __ldcg(src + v);
+    }
+    T *y = Y + (int64_t)r * ldy + (int64_t)f * VW;
+    Frag<T, VW> cur;
+    cur.load(y);
+#pragma unroll
+    for (int v = 0; v < VW; ++v) acc[v] += cur.get(v);
+    store_frag<T, VW>(y, acc);
+  }
+}
+
+// ---------------------------------------------------------------- dispatch
+
+template <typename T, int VW>
+cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
+                    const float *vals, const T *X, int64_t ldx, T *Y, int64_t ldy,
+                    const ChunkList &cl, float *partial, cudaStream_t s) {
+  const int64_t per_block = (kBlock / 32) * (32 / (g.G * g.E));
+  const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
+  const int64_t row_blocks = (n_rows + per_block - 1) / per_block;
+  const int64_t grid = chunk_blocks + row_blocks;
+  if (grid > 0) {
+#define AUTOSAGE_SPMM_NV(NVV)                                                                     \
+  spmm_rows_kernel<T, VW, NVV><<<(unsigned)grid, kBlock, 0, s>>>(                               \
+      n_rows, row_ptr, col_idx, vals, g.H, g.es, g.cph, X, ldx, Y, ldy, g.nfrag, g.G, g.E, cl,    \
+      chunk_blocks, partial)
+    switch (g.NV) {
+      case 1: AUTOSAGE_SPMM_NV(1); break;
+      case 2: AUTOSAGE_SPMM_NV(2); break;
+      case 4: AUTOSAGE_SPMM_NV(4); break;
+      case 8: AUTOSAGE_SPMM_NV(8); break;
+      case 16: AUTOSAGE_SPMM_NV(16); break;
+      default: return cudaErrorInvalidValue;
+    }
+#undef AUTOSAGE_SPMM_NV
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (cl.n_long > 0) {
+    const unsigned fgrid = (unsigned)((cl.n_long + kBlock / 32 - 1) / (kBlock / 32));
+    spmm_fixup_kernel<T, VW><<<fgrid, kBlock, 0, s>>>(cl, g.nfrag, partial, Y, ldy);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+template <typename T, int VW>
+cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                         const int32_t *col_idx, const float *vals, const T *X, int64_t ldx, T *Y,
+                         int64_t ldy, const int2 *part, int64_t n_warps, float *carry_val,
+                         int32_t *carry_row, cudaStream_t s) {
+  if (n_warps <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((n_warps + kBlock / 32 - 1) / (kBlock / 32));
+#define AUTOSAGE_MP_NV(NVV)                                                                         \
+  spmm_mergepath_kernel<T, VW, NVV><<<grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, vals, X, ldx, \
+                                                           Y, ldy, g.nfrag, g.G, g.E, part,        \
+                                                           n_warps, carry_val, carry_row)
+  switch (g.NV) {
+    case 1: AUTOSAGE_MP_NV(1); break;
+    case 2: AUTOSAGE_MP_NV(2); break;
+    case 4: AUTOSAGE_MP_NV(4); break;
+    case 8: AUTOSAGE_MP_NV(8); break;
+    case 16: AUTOSAGE_MP_NV(16); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef AUTOSAGE_MP_NV
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  mergepath_fixup_kernel<T, VW><<<grid, kBlock, 0, s>>>(n_warps, g.nfrag, carry_val, carry_row, Y, ldy);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_spmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                        const int32_t *col_idx, const float *vals, const void *X, int64_t ldx,
+                        void *Y, int64_t ldy, const ChunkList &cl, float *partial,
+                        cudaStream_t s) {
+  if (g.dt == DType::F32) {
+    auto x = static_cast<const float *>(X);
+    auto y = static_cast<float *>(Y);
+    switch (g.VW) {
+      case 4: return spmm_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+      case 2: return spmm_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+      case 1: return spmm_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+    }
+  } else {
+    auto x = static_cast<const __nv_bfloat16 *>(X);
+    auto y = static_cast<__nv_bfloat16 *>(Y);
+    switch (g.VW) {
+      case 8: return spmm_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+      case 4: return spmm_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+      case 2: return spmm_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+      case 1: return spmm_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mergepath_partition(int64_t n_rows, int64_t nnz, const int32_t *row_ptr,
+                                       int64_t items, int64_t n_warps, int2 *part, cudaStream_t s) {
+  const int64_t n = n_warps + 1;
+  mergepath_partition_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(n_rows, nnz, row_ptr, items,
+                                                                          n_warps, part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_spmm_mergepath(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
+                                  const int32_t *col_idx, const float *vals, const void *X,
+                                  int64_t ldx, void *Y, int64_t ldy, const int2 *part,
+                                  int64_t n_warps, float *carry_val, int32_t *carry_row,
+                                  cudaStream_t s) {
+  if (g.G * g.E != 32) return cudaErrorInvalidValue;
+  if (g.dt == DType::F32) {
+    auto x = static_cast<const float *>(X);
+    auto y = static_cast<float *>(Y);
+    switch (g.VW) {
+      case 4: return mergepath_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 2: return mergepath_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 1: return mergepath_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+    }
+  } else {
+    auto x = static_cast<const __nv_bfloat16 *>(X);
+    auto y = static_cast<__nv_bfloat16 *>(Y);
+    switch (g.VW) {
+      case 8: return mergepath_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 4: return mergepath_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 2: return mergepath_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 1: return mergepath_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace autosage

@@ -128,15 +128,28 @@ def rmat(scale: int, edge_factor: int = 16, a: float = 0.57, b: float = 0.19,
     m = edge_factor * n
     u = np.zeros(m, dtype=np.int64)
     v = np.zeros(m, dtype=np.int64)
-    ab, abc = a + b, a + b + c
-    for level in range(scale):
-        r = rng.random(m, dtype=np.float32)
-        bit = np.int64(1 << (scale - 1 - level))
-        # quadrant: [0,a) -> (0,0); [a,a+b) -> (0,1); [a+b,a+b+c) -> (1,0); else (1,1)
-        u += bit * (r >= ab)
-        v += bit * (((r >= a) & (r < ab)) | (r >= abc))
-    keys = np.unique(u * n + v)
-    return _csr_from_sorted_keys(keys, n, n)
+    ab, abc = np.float32(a + b), np.float32(a + b + c)
+    fa = np.float32(a)
+    block = 1 << 18  # edges per block: keeps the per-level temporaries in cache
+    for s0 in range(0, m, block):
+        s1 = min(m, s0 + block)
+        r = rng.random((scale, s1 - s0), dtype=np.float32)  # one row of draws per bit level
+        ub = np.zeros(s1 - s0, dtype=np.int64)
+        vb = np.zeros(s1 - s0, dtype=np.int64)
+        for level in range(scale):
+            rl = r[level]
+            # quadrant: [0,a) -> (0,0); [a,a+b) -> (0,1); [a+b,a+b+c) -> (1,0); else (1,1)
+            ub <<= 1
+            vb <<= 1
+            ub |= rl >= ab
+            vb |= ((rl >= fa) & (rl < ab)) | (rl >= abc)
+        u[s0:s1] = ub
+        v[s0:s1] = vb
+    keys = u * n + v
+    keys.sort()
+    keep = np.ones(keys.shape[0], dtype=bool)
+    keep[1:] = keys[1:] != keys[:-1]
+    return _csr_from_sorted_keys(keys[keep], n, n)
 
 
 def uniform_degree(n: int, nnz: int, seed: int = 0) -> Csr:

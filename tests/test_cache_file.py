@@ -1,0 +1,81 @@
+"""Persistent plan cache file handling on the host (no GPU): round trip,
+bad header, corrupt and truncated lines are skipped with a status, never a crash."""
+import os
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def sga():
+    from sparse_gnn_aggregation_gb300 import build
+    build.build()
+    import sparse_gnn_aggregation_gb300 as m
+    return m
+
+
+HEADER = "# autosage plan cache v1\n"
+GOOD = "NVIDIA_GB300|sm152|op0|dt0|F64|H1|n10|m10|nnz20|fp00000000000000ab\tsplit 16 2 512 0.123000\n"
+
+
+def test_round_trip(tmp_path, sga):
+    sga.autosage_cache_clear()
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + GOOD)
+    sga.autosage_cache_load(str(p))
+    assert sga.autosage_cache_size() == 1
+    q = tmp_path / "d.txt"
+    sga.autosage_cache_save(str(q))
+    assert q.read_text() == HEADER + GOOD
+    sga.autosage_cache_clear()
+    assert sga.autosage_cache_size() == 0
+
+
+def test_wrong_header_rejected(tmp_path, sga):
+    sga.autosage_cache_clear()
+    p = tmp_path / "c.txt"
+    p.write_text("# autosage plan cache v0\n" + GOOD)
+    with pytest.raises(sga.AutosageError) as e:
+        sga.autosage_cache_load(str(p))
+    assert e.value.status == sga.ERR_CACHE_FORMAT
+    assert sga.autosage_cache_size() == 0
+
+
+@pytest.mark.parametrize("bad", [
+    "no-tab-here split 16 2 512 0.1\n",
+    "key\tsplit 16 2\n",                       # truncated
+    "key\twarp 16 2 512 0.1\n",                # unknown schedule
+    "key\trowgroup 3 1 0 0.1\n",               # lanes not a power of two
+    "key\tsplit 16 4 0 0.1\n",                 # split schedule without a chunk length
+    "key\trowgroup 16 4 0 0.1 extra\n",        # trailing field
+    "\tsplit 16 2 512 0.1\n",                  # empty key
+])
+def test_corrupt_lines_are_skipped(tmp_path, sga, bad):
+    sga.autosage_cache_clear()
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + bad + GOOD)
+    with pytest.raises(sga.AutosageError) as e:
+        sga.autosage_cache_load(str(p))
+    assert e.value.status == sga.ERR_CACHE_FORMAT
+    assert sga.autosage_cache_size() == 1  # the good line still loaded
+
+
+def test_truncated_file_and_missing_file(tmp_path, sga):
+    sga.autosage_cache_clear()
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + GOOD[: len(GOOD) // 2])
+    with pytest.raises(sga.AutosageError):
+        sga.autosage_cache_load(str(p))
+    assert sga.autosage_cache_size() == 0
+    with pytest.raises(sga.AutosageError) as e:
+        sga.autosage_cache_load(str(tmp_path / "missing.txt"))
+    assert e.value.status == sga.ERR_CACHE_IO
+
+
+def test_save_is_atomic_replace(tmp_path, sga):
+    sga.autosage_cache_clear()
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + GOOD)
+    sga.autosage_cache_load(str(p))
+    sga.autosage_cache_save(str(p))
+    assert not os.path.exists(str(p) + ".tmp")
+    assert p.read_text() == HEADER + GOOD

@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry point
+that include/autosage.h declares (no compute calls here)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "autosage.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(autosage_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    import shutil
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from sparse_gnn_aggregation_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_north_star_api():
+    syms = declared_symbols()
+    for name in ("autosage_spmm", "autosage_sddmm", "autosage_csr_attention", "autosage_plan",
+                 "autosage_plan_destroy", "autosage_cache_load", "autosage_cache_save",
+                 "autosage_status_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True, check=True)
+    exported = {line.split()[-1] for line in out.stdout.splitlines() if line.strip()}
+    missing = [s for s in declared_symbols() if s not in exported]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_binding_loads_and_names_match(lib_path):
+    import sparse_gnn_aggregation_gb300 as sga
+    assert sorted(sga.EXPORTS) == declared_symbols()
+    for name in sga.EXPORTS:
+        assert hasattr(sga.library(), name)
+        if name not in ("autosage_status_string", "autosage_last_error", "autosage_version", "autosage_plan_destroy",
+                        "autosage_cache_clear", "autosage_cache_size", "autosage_plan_describe",
+                        "autosage_plan_schedule"):
+            assert hasattr(sga, name), f"binding lacks {name}"
+    assert sga.autosage_version().startswith("autosage-gb300")
+    assert sga.library().autosage_status_string(sga.ERR_PROBE).decode().startswith("every probed")
+
+
+def test_host_side_argument_checks_need_no_gpu(lib_path):
+    """Calls rejected on the host return a status before touching the device."""
+    import ctypes
+    import sparse_gnn_aggregation_gb300 as sga
+    lib = sga.library()
+    assert lib.autosage_spmm(None, None, 0, None, 0, 4, 0, 0, None, None) == sga.ERR_INVALID_ARG
+    assert b"A is NULL" in lib.autosage_last_error()
+    c = sga._Csr(-1, 4, 0, 16, 0, 0)
+    assert lib.autosage_sddmm(ctypes.byref(c), None, 0, None, 0, 4, 0, 1.0, None, None, None) == sga.ERR_INVALID_ARG
+    c = sga._Csr(4, 4, 0, 16, 0, 0)  # row_ptr "pointer" 16, F = 0
+    assert lib.autosage_spmm(ctypes.byref(c), None, 0, None, 0, 0, 0, 0, None, None) == sga.ERR_INVALID_ARG
+    assert lib.autosage_cache_load(b"/nonexistent/dir/cache.txt") == sga.ERR_CACHE_IO
+    sched = sga._Schedule(sga.SCHED_ROWGROUP, 3, 1, 0)  # lanes not a power of two
+    h = ctypes.c_void_p()
+    assert lib.autosage_plan_with_schedule(ctypes.byref(c), 0, 4, 1, 0, ctypes.byref(sched), ctypes.byref(h),
+                                           None) == sga.ERR_INVALID_ARG
