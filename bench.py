@@ -88,8 +88,8 @@ def traffic_for(op_key: str):
 
 # ---------------------------------------------------------------- workload
 
-def build_graphs():
-    rm = synth.rmat_skew(20, seed=0)
+def build_graphs(scale: int = 20):
+    rm = synth.rmat_skew(scale, seed=0)
     un = synth.uniform_control(rm, seed=0)
     return {"rmat": rm, "uniform": un}
 
@@ -109,9 +109,9 @@ def attn_bytes(n, nnz, H, D, s, fused):
     return b
 
 
-def op_list(graphs):
+def op_list(graphs, only=None):
     """(key, kind, graph, F) in execution order; graphs alternate so the other
-    graph's data sits between two uses of one CSR."""
+    graph's data sits between two uses of one CSR. `only` keeps keys containing it."""
     ops = []
     for F in FS:
         for gname in ("rmat", "uniform"):
@@ -121,6 +121,8 @@ def op_list(graphs):
     ops.append(("spmm_t/rmat/F64", "spmm_t", "rmat", 64))
     ops.append(("attn_fused/rmat/H8D64", "attn_fused", "rmat", HEAD_DIM))
     ops.append(("attn_unfused/rmat/H8D64", "attn_unfused", "rmat", HEAD_DIM))
+    if only:
+        ops = [o for o in ops if only in o[0]]
     return ops
 
 
@@ -198,9 +200,11 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    graphs = build_graphs()
-    ops = op_list(graphs)
+    graphs = build_graphs(args.scale)
+    ops = op_list(graphs, args.only)
     stream = torch.cuda.current_stream()
+    if args.cache and os.path.exists(args.cache):
+        sga.autosage_cache_load(args.cache)
     mats = {k: sga.CsrMatrix.from_numpy(g.row_ptr, g.col_idx, g.vals, g.n_cols) for k, g in graphs.items()}
     # resident inputs (one per width so nothing is shared between operations)
     feats, host_feats = {}, {}
@@ -232,6 +236,8 @@ def run_ours(args):
             plans[key] = sga.autosage_plan(A, sga.OP_ATTN_UNFUSED, F, heads=HEADS, dtype=torch.bfloat16,
                                            flags=flags)
     plan_s = time.perf_counter() - t_plan
+    if args.cache:
+        sga.autosage_cache_save(args.cache)
 
     def run(key, kind, gname, F, f, out=None):
         A, P = mats[gname], plans[key]
@@ -384,6 +390,8 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if args.scale != 20 or args.only:
+        line["config"]["workload"] = f"PARTIAL (scale {args.scale}, only={args.only}); not the benchmark workload"
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(graphs, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -457,7 +465,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    graphs = build_graphs()
+    graphs = build_graphs(args.scale)
     budget = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_baseline(graphs, budget_s=budget)
@@ -484,6 +492,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--only", default=None, help="run only operations whose key contains this text")
+    ap.add_argument("--scale", type=int, default=20, help="R-MAT scale (20 is the benchmark workload)")
+    ap.add_argument("--cache", default=None, help="plan cache file: loaded if present, saved after planning")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

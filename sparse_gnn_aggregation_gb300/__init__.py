@@ -2,9 +2,10 @@
 
 Argument marshalling only: every step runs in the library's CUDA kernels
 behind the C ABI in ``include/autosage.h``. PyTorch supplies device memory
-and the current stream; there is no CPU or vendor-library path. Importing
-this package raises if the native library has not been built (run
-``python -m sparse_gnn_aggregation_gb300.build`` or ``__graft_entry__.build()``).
+and the current stream; there is no CPU or vendor-library path. Nothing
+works until the native library is built (run
+``python -m sparse_gnn_aggregation_gb300.build`` or ``__graft_entry__.build()``):
+the first call into the library raises ImportError.
 
 Operations (AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN
 Aggregation (SpMM/SDDMM) and CSR Attention", Abstract): SpMM, SDDMM, the
@@ -97,7 +98,18 @@ def _load():
     return lib
 
 
-_lib = _load()
+class _LazyLib:
+    """Loads libautosage.so on first use; raises ImportError if it is not built."""
+
+    _handle = None
+
+    def __getattr__(self, name):
+        if _LazyLib._handle is None:
+            _LazyLib._handle = _load()
+        return getattr(_LazyLib._handle, name)
+
+
+_lib = _LazyLib()
 
 
 def _check(status: int):
@@ -355,4 +367,5 @@ def autosage_version() -> str:
 
 def library():
     """The loaded ctypes library (for symbol checks)."""
-    return _lib
+    _lib.autosage_version  # force the load
+    return _LazyLib._handle

@@ -57,14 +57,17 @@ __global__ void __launch_bounds__(kBlock) attention_kernel(
     for (int v = 0; v < VW; ++v) acc[k][v] = 0.f;
   }
   constexpr int U = NV * VW <= 8 ? 4 : 2;
+  int c[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int q = it.b + L.e + u * E;
+    c[u] = q < it.e ? ld_stream_i32(col_idx + q) : 0;
+  }
   for (int p = it.b + L.e; p < it.e; p += U * E) {
-    int c[U];
     bool live[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      live[u] = p + u * E < it.e;
-      c[u] = live[u] ? ld_stream_i32(col_idx + p + u * E) : 0;
-    }
+    for (int u = 0; u < U; ++u) live[u] = p + u * E < it.e;
+    int cn[U];  // next iteration's columns, fetched while this iteration's rows are in flight
     Frag<T, VW> fv[U][NV];
     float s[U][NV];
     if constexpr (GIVEN) {
@@ -85,6 +88,11 @@ __global__ void __launch_bounds__(kBlock) attention_kernel(
 #pragma unroll
         for (int k = 0; k < NV; ++k)
           if (live[u] && valid[k]) fv[u][k].load(V + (int64_t)c[u] * ld + (int64_t)(g + k * G) * VW);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = p + U * E + u * E;
+        cn[u] = q < it.e ? ld_stream_i32(col_idx + q) : 0;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float hs[NV];
@@ -114,6 +122,11 @@ __global__ void __launch_bounds__(kBlock) attention_kernel(
 #pragma unroll
         for (int k = 0; k < NV; ++k)
           if (live[u] && valid[k]) fv[u][k].load(V + (int64_t)c[u] * ld + (int64_t)(g + k * G) * VW);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int q = p + U * E + u * E;
+        cn[u] = q < it.e ? ld_stream_i32(col_idx + q) : 0;
+      }
     }
     // online softmax update with U new scores per fragment slot
 #pragma unroll
@@ -139,6 +152,8 @@ __global__ void __launch_bounds__(kBlock) attention_kernel(
       }
       m[k] = mx;
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u) c[u] = cn[u];
   }
   // merge the E edge-lane states (fixed xor order)
   for (int off = G; off < L.GE; off <<= 1) {

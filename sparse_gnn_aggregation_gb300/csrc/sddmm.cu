@@ -21,20 +21,25 @@ __device__ __forceinline__ void sddmm_edges(const Lanes &L, const int32_t *__res
                                             int cph, int mshift, int R, float *__restrict__ S, int p0,
                                             int pe) {
   const int G = L.G, E = L.E, g = L.g;
+  int c[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) c[u] = p0 + u * E < pe ? ld_stream_i32(col_idx + p0 + u * E) : 0;
   for (int p = p0; p < pe; p += U * E) {
-    int c[U];
     bool live[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      live[u] = p + u * E < pe;
-      c[u] = live[u] ? ld_stream_i32(col_idx + p + u * E) : 0;
-    }
+    for (int u = 0; u < U; ++u) live[u] = p + u * E < pe;
     Frag<T, VW> f[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int k = 0; k < NV; ++k)
         if (live[u] && g + k * G < nfrag) f[u][k].load(K + (int64_t)c[u] * ldk + (int64_t)(g + k * G) * VW);
+    // next iteration's columns are fetched while these rows are in flight
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = p + U * E + u * E;
+      c[u] = q < pe ? ld_stream_i32(col_idx + q) : 0;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       // partial dot per fragment slot, summed into head groups of 2^mshift slots

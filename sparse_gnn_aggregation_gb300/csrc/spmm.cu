@@ -26,7 +26,34 @@ __device__ __forceinline__ void zero(float (&acc)[NV][VW]) {
     for (int v = 0; v < VW; ++v) acc[k][v] = 0.f;
 }
 
+// Edge weights of U edges p, p + E, ... for every fragment slot.
+template <int U, int NV>
+__device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx,
+                                             const float *__restrict__ vals, int H, int es,
+                                             const int (&head)[NV], int p, int E, int (&c)[U],
+                                             float (&w)[U][NV]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) c[u] = ld_stream_i32(col_idx + p + u * E);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (vals == nullptr) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) w[u][k] = 1.f;
+    } else if (H == 1) {
+      const float x = ld_stream_f32(vals + (int64_t)(p + u * E) * es);
+#pragma unroll
+      for (int k = 0; k < NV; ++k) w[u][k] = x;
+    } else {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) w[u][k] = __ldg(vals + (int64_t)(p + u * E) * es + head[k]);
+    }
+  }
+}
+
 // Accumulate edges p = p0, p0 + E, ... < pe into acc (per lane fragments).
+// Full iterations take U edges per edge lane; the next iteration's column
+// indices and weights are loaded while this iteration's rows are in flight,
+// so each iteration waits on one memory round trip, not two.
 template <typename T, int VW, int NV, int U>
 __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx,
                                              const float *__restrict__ vals, int H, int es,
@@ -35,38 +62,38 @@ __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx
                                              int pe, float (&acc)[NV][VW]) {
   int p = p0;
   if constexpr (U > 1) {
-    for (; p + (U - 1) * E < pe; p += U * E) {
+    if (p + (U - 1) * E < pe) {
       int c[U];
       float w[U][NV];
+      load_weights<U, NV>(col_idx, vals, H, es, head, p, E, c, w);
+      while (true) {
+        Frag<T, VW> f[U][NV];
 #pragma unroll
-      for (int u = 0; u < U; ++u) c[u] = ld_stream_i32(col_idx + p + u * E);
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (vals == nullptr) {
+          for (int k = 0; k < NV; ++k)
+            if (g + k * G < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)(g + k * G) * VW);
+        const int pn = p + U * E;
+        const bool more = pn + (U - 1) * E < pe;
+        int cn[U];
+        float wn[U][NV];
+        if (more) load_weights<U, NV>(col_idx, vals, H, es, head, pn, E, cn, wn);
 #pragma unroll
-          for (int k = 0; k < NV; ++k) w[u][k] = 1.f;
-        } else if (H == 1) {
-          const float x = ld_stream_f32(vals + (int64_t)(p + u * E) * es);
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int k = 0; k < NV; ++k) w[u][k] = x;
-        } else {
+          for (int k = 0; k < NV; ++k)
+            if (g + k * G < nfrag)
 #pragma unroll
-          for (int k = 0; k < NV; ++k) w[u][k] = __ldg(vals + (int64_t)(p + u * E) * es + head[k]);
+              for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[u][k], f[u][k].get(v), acc[k][v]);
+        p = pn;
+        if (!more) break;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          c[u] = cn[u];
+#pragma unroll
+          for (int k = 0; k < NV; ++k) w[u][k] = wn[u][k];
         }
       }
-      Frag<T, VW> f[U][NV];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (g + k * G < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)(g + k * G) * VW);
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (g + k * G < nfrag)
-#pragma unroll
-            for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[u][k], f[u][k].get(v), acc[k][v]);
     }
   }
   for (; p < pe; p += E) {
