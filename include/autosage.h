@@ -141,6 +141,29 @@ autosage_status autosage_edge_softmax_aggregate(const autosage_csr *A, const flo
                                                 autosage_dtype dt, void *out,
                                                 autosage_plan_t plan, void *stream);
 
+/* Unfused CSR attention that allocates no device memory. This entry point has no
+ * counterpart in the paper; it is for callers that must not allocate inside their
+ * work loop (a serving process that reserved all device memory for its own pool,
+ * or a latency-critical loop where a driver allocation could synchronise the
+ * device). It computes what autosage_csr_attention(fused = 0, plan = NULL)
+ * computes, with the same kernels, but keeps the fp32 score array in a fixed
+ * device array owned by the library: AUTOSAGE_NOALLOC_MAX_SCORES fp32 elements
+ * (16 MiB), held on every GPU the library is loaded on until the process exits.
+ *  - nnz * heads above AUTOSAGE_NOALLOC_MAX_SCORES returns AUTOSAGE_ERR_UNSUPPORTED
+ *    before any launch; no cudaMalloc / cudaFree or allocating routine is called.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array and leaves its scores there.
+ *    Calls whose work overlaps on the GPU (other streams, other threads) race on
+ *    it: serialise them. Nothing in the array needs to start at zero.
+ * Arguments as autosage_csr_attention (Q/K/V/out [n, heads, D] of type dt). */
+#define AUTOSAGE_NOALLOC_MAX_SCORES (4u * 1024u * 1024u)
+autosage_status autosage_csr_attention_unfused_noalloc(const autosage_csr *A, const void *Q,
+                                                       const void *K, const void *V, int heads,
+                                                       int64_t D, autosage_dtype dt, float scale,
+                                                       void *out, void *stream);
+
 /* ---------------------------------------------------------------- planning */
 
 /* Build a plan for (A, op, F, heads, dt). For attention ops F is the head dimension D.

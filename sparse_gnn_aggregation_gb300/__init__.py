@@ -38,6 +38,7 @@ EXPORTS = [
     "autosage_cache_load", "autosage_cache_save", "autosage_cache_clear", "autosage_cache_size",
     "autosage_row_stats", "autosage_fingerprint", "autosage_validate_csr", "autosage_csr_transpose",
     "autosage_status_string", "autosage_last_error", "autosage_version",
+    "autosage_csr_attention_unfused_noalloc",
 ]
 
 
@@ -69,6 +70,7 @@ def _load():
         "autosage_sddmm": [CSR, P, I64, P, I64, I64, I, F, P, P, P],
         "autosage_row_softmax": [CSR, P, I, P, P],
         "autosage_csr_attention": [CSR, P, P, P, I, I64, I, F, P, I, P, P],
+        "autosage_csr_attention_unfused_noalloc": [CSR, P, P, P, I, I64, I, F, P, P],
         "autosage_edge_softmax_aggregate": [CSR, P, P, I, I64, I, P, P, P],
         "autosage_plan": [CSR, I, I64, I, I, U, ctypes.POINTER(P), P],
         "autosage_plan_with_schedule": [CSR, I, I64, I, I, ctypes.POINTER(_Schedule), ctypes.POINTER(P), P],
@@ -295,6 +297,27 @@ def autosage_csr_attention(A: CsrMatrix, Q, K, V, heads: int, scale: float, fuse
             raise ValueError("attention tensors must be contiguous")
     _check(_lib.autosage_csr_attention(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), D, _dt(Q), float(scale),
                                        _ptr(out), int(bool(fused)), _plan_handle(plan), _stream(stream)))
+    return out
+
+
+NOALLOC_MAX_SCORES = 4 * 1024 * 1024
+
+
+def autosage_csr_attention_unfused_noalloc(A: CsrMatrix, Q, K, V, heads: int, scale: float, out, stream=None):
+    """Unfused CSR attention that allocates no device memory in the library.
+
+    For callers that must not allocate inside their work loop. The caller
+    passes every input and the output (``out`` is required); the score array
+    lives in a fixed 16 MiB device array inside the library, so nnz * heads
+    may not exceed NOALLOC_MAX_SCORES. Calls that overlap on the GPU share
+    that array and must be serialised by the caller.
+    """
+    W = int(Q.shape[-1]) if Q.dim() == 2 else int(Q.shape[-1] * Q.shape[-2])
+    for t in (Q, K, V, out):
+        if not t.is_contiguous():
+            raise ValueError("attention tensors must be contiguous")
+    _check(_lib.autosage_csr_attention_unfused_noalloc(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), W // heads,
+                                                       _dt(Q), float(scale), _ptr(out), _stream(stream)))
     return out
 
 

@@ -1339,3 +1339,34 @@ autosage_status autosage_cache_load(const char *path) {
 }
 
 }  // extern "C"
+
+namespace autosage {
+// Record a status with a message for autosage_last_error().
+autosage_status report(autosage_status st, const char *msg) { return fail(st, "%s", msg); }
+}  // namespace autosage
+
+// Unfused CSR attention with a caller-supplied fp32 score buffer of at least
+// nnz * heads elements, default schedule, no plan, no device allocation.
+namespace autosage {
+autosage_status attention_unfused_with_scores(const autosage_csr *A, const void *Q, const void *K,
+                                              const void *V, int heads, int64_t D, autosage_dtype dt,
+                                              float scale, void *out, float *scores, cudaStream_t s) {
+  if (!A) return fail(AUTOSAGE_ERR_INVALID_ARG, "A is NULL");
+  if (A->n_rows < 0 || A->n_cols < 0 || A->nnz < 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "negative CSR size");
+  if (!A->row_ptr || (A->nnz > 0 && !A->col_idx)) return fail(AUTOSAGE_ERR_INVALID_ARG, "CSR pointer is NULL");
+  if (A->nnz > 0 && A->n_cols == 0) return fail(AUTOSAGE_ERR_INVALID_CSR, "edges but no columns");
+  if (heads < 1 || D < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads and D must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  const int64_t W = (int64_t)heads * D;
+  autosage_status st;
+  if ((st = check_mat(Q, W, W, A->n_rows, "Q")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(K, W, W, A->n_cols, "K")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(V, W, W, A->n_cols, "V")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(out, W, W, A->n_rows, "out")) != AUTOSAGE_OK) return st;
+  if (A->n_rows == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.Q = Q; a.K = K; a.X = V; a.Y = out; a.alpha = scale; a.S = scores;
+  autosage_plan_s P = transient(A, AUTOSAGE_OP_ATTN_UNFUSED, D, heads, dt);
+  return run_op(&P, AUTOSAGE_OP_ATTN_UNFUSED, a, s);
+}
+}  // namespace autosage
