@@ -20,157 +20,186 @@ namespace autosage {
 
 namespace {
 
-template <typename T, int VW, int NV, bool GIVEN>
-__global__ void __launch_bounds__(kBlock) attention_kernel(
+// Scores more than kRescale above the running reference m trigger a rescale
+// of (l, acc) to the new maximum; smaller increases keep the old reference,
+// so exp(s - m) stays below e^kRescale and the common case skips the rescale.
+// The result acc / l does not depend on which reference was used.
+constexpr float kRescale = 8.f;
+
+// Fragment slot k of lane g covers fragment g * fs + k * ks: fs = 1, ks = G
+// interleaves lanes (one coalesced load per slot); fs = NV, ks = 1 gives each
+// lane NV consecutive fragments, which keeps a lane inside one head.
+// ONE: all of a lane's slots belong to one head (single-head rows, or
+// consecutive fragments within a head): one running (m, l) and one exp per
+// edge. Otherwise every slot is its own head (interleaved lanes, heads of
+// at most G fragments). R lanes share a head and finish its dot product with
+// xor shuffles.
+// Blocks per SM the register budget is sized for: lanes holding few values
+// (bf16 up to 16, fp32 up to 4) leave room for three 256-thread blocks
+// (85 registers per thread); wider ones get two.
+template <typename T, int VW, int NV>
+constexpr int attn_min_blocks() {
+  return (NV * VW <= 4 || (sizeof(T) == 2 && NV * VW <= 16)) ? 3 : 2;
+}
+
+template <typename T, int VW, int NV, bool GIVEN, bool ONE>
+__global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attention_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, const T *__restrict__ K, const float *__restrict__ scores,
-    const T *__restrict__ V, int64_t ld, float scale, int H, int es, int cph, int mshift, int R, int nfrag,
-    int G, int E, T *__restrict__ O, ChunkList cl, int64_t chunk_blocks,
+    const T *__restrict__ V, int64_t ld, float scale, int H, int es, int cph, int R, int nfrag,
+    int G, int E, int fs, int ks, T *__restrict__ O, ChunkList cl, int64_t chunk_blocks,
     float *__restrict__ part_acc, float *__restrict__ part_ml) {
+  constexpr int NG = ONE ? 1 : NV;  // head groups per lane
   const Lanes L(G, E);
   const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
   const int g = L.g;
   bool valid[NV];
-  int head[NV];
+  int frag[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    valid[k] = g + k * G < nfrag;
-    head[k] = (H > 1 && valid[k]) ? (g + k * G) / cph : 0;
+    frag[k] = g * fs + k * ks;
+    valid[k] = frag[k] < nfrag;
   }
-  float q[NV][VW];
+  int head[NG];
+#pragma unroll
+  for (int j = 0; j < NG; ++j) head[j] = (H > 1 && frag[j] < nfrag) ? frag[j] / cph : 0;
+  // the row's Q fragments stay packed (bf16 halves the registers); the scale
+  // is applied to the finished dot product
+  Frag<T, VW> q[NV];
   if constexpr (!GIVEN) {
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      Frag<T, VW> f;
-      const bool ok = it.e > it.b && valid[k];
-      if (ok) f.load(Q + it.row * ld + (int64_t)(g + k * G) * VW);
-#pragma unroll
-      for (int v = 0; v < VW; ++v) q[k][v] = ok ? scale * f.get(v) : 0.f;
+      if (it.e > it.b && valid[k])
+        q[k].load(Q + it.row * ld + (int64_t)frag[k] * VW);
+      else
+        q[k].zero();
     }
   }
-  float m[NV], l[NV], acc[NV][VW];
+  float m[NG], l[NG], acc[NV][VW];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    m[k] = -INFINITY;
-    l[k] = 0.f;
+  for (int j = 0; j < NG; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
 #pragma unroll
     for (int v = 0; v < VW; ++v) acc[k][v] = 0.f;
-  }
   constexpr int U = NV * VW <= 8 ? 4 : 2;
   int c[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int q = it.b + L.e + u * E;
-    c[u] = q < it.e ? ld_stream_i32(col_idx + q) : 0;
+    const int qe = it.b + L.e + u * E;
+    c[u] = qe < it.e ? ld_stream_i32(col_idx + qe) : 0;
   }
   for (int p = it.b + L.e; p < it.e; p += U * E) {
     bool live[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) live[u] = p + u * E < it.e;
-    int cn[U];  // next iteration's columns, fetched while this iteration's rows are in flight
     Frag<T, VW> fv[U][NV];
-    float s[U][NV];
+    float s[U][NG];
     if constexpr (GIVEN) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
+        for (int j = 0; j < NG; ++j)
+          s[u][j] = live[u] ? __ldg(scores + (int64_t)(p + u * E) * es + head[j]) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
         for (int k = 0; k < NV; ++k)
-          s[u][k] = live[u] ? __ldg(scores + (int64_t)(p + u * E) * es + head[k]) : -INFINITY;
+          if (live[u] && valid[k]) fv[u][k].load(V + (int64_t)c[u] * ld + (int64_t)frag[k] * VW);
     } else {
       Frag<T, VW> fk[U][NV];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-          if (live[u] && valid[k]) fk[u][k].load(K + (int64_t)c[u] * ld + (int64_t)(g + k * G) * VW);
+          if (live[u] && valid[k]) fk[u][k].load(K + (int64_t)c[u] * ld + (int64_t)frag[k] * VW);
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-          if (live[u] && valid[k]) fv[u][k].load(V + (int64_t)c[u] * ld + (int64_t)(g + k * G) * VW);
+          if (live[u] && valid[k]) fv[u][k].load(V + (int64_t)c[u] * ld + (int64_t)frag[k] * VW);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int q = p + U * E + u * E;
-        cn[u] = q < it.e ? ld_stream_i32(col_idx + q) : 0;
-      }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float hs[NV];
-#pragma unroll
-        for (int k = 0; k < NV; ++k) hs[k] = 0.f;
+        for (int j = 0; j < NG; ++j) s[u][j] = 0.f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
           if (valid[k]) {
             float d = 0.f;
 #pragma unroll
-            for (int v = 0; v < VW; ++v) d = fmaf(q[k][v], fk[u][k].get(v), d);
-            hs[k >> mshift] += d;
+            for (int v = 0; v < VW; ++v) d = fmaf(q[k].get(v), fk[u][k].get(v), d);
+            s[u][ONE ? 0 : k] += d;
           }
         }
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          if ((j << mshift) >= NV) break;
-          for (int off = 1; off < R; off <<= 1) hs[j] += __shfl_xor_sync(L.sub_mask, hs[j], off);
+        for (int j = 0; j < NG; ++j) {
+          for (int off = 1; off < R; off <<= 1) s[u][j] += __shfl_xor_sync(L.sub_mask, s[u][j], off);
+          s[u][j] = live[u] ? scale * s[u][j] : -INFINITY;
         }
-#pragma unroll
-        for (int k = 0; k < NV; ++k) s[u][k] = live[u] ? hs[k >> mshift] : -INFINITY;
       }
     }
-    if constexpr (GIVEN) {
+    // next iteration's columns, fetched while this iteration's rows are in flight
 #pragma unroll
-      for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
+      const int qe = p + U * E + u * E;
+      c[u] = qe < it.e ? ld_stream_i32(col_idx + qe) : 0;
+    }
+    // online softmax per head group, with a lazily moved reference maximum
+    float w[U][NG];
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      float mx = s[0][j];
+#pragma unroll
+      for (int u = 1; u < U; ++u) mx = fmaxf(mx, s[u][j]);
+      if (mx > m[j] + kRescale) {  // m[j] = -inf: the first finite score sets the reference
+        const float corr = __expf(m[j] - mx);
+        l[j] *= corr;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-          if (live[u] && valid[k]) fv[u][k].load(V + (int64_t)c[u] * ld + (int64_t)(g + k * G) * VW);
+          if (ONE || k == j)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) acc[k][v] *= corr;
+        m[j] = mx;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int q = p + U * E + u * E;
-        cn[u] = q < it.e ? ld_stream_i32(col_idx + q) : 0;
+        w[u][j] = (live[u] && m[j] != -INFINITY) ? __expf(s[u][j] - m[j]) : 0.f;
+        l[j] += w[u][j];
       }
     }
-    // online softmax update with U new scores per fragment slot
+    // rows of edges that are not live were never loaded: skip them (0 * garbage may be NaN)
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      float mx = m[k];
+    for (int k = 0; k < NV; ++k)
+      if (valid[k])
 #pragma unroll
-      for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][k]);
-      // m[k] = -inf (first edges) gives 0; an all -inf set of scores leaves the state as is
-      const float corr = mx == -INFINITY ? 1.f : __expf(m[k] - mx);
-      l[k] *= corr;
+        for (int u = 0; u < U; ++u)
+          if (live[u])
 #pragma unroll
-      for (int v = 0; v < VW; ++v) acc[k][v] *= corr;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (live[u]) {
-          const float w = mx == -INFINITY ? 0.f : __expf(s[u][k] - mx);
-          l[k] += w;
-          if (valid[k]) {
-#pragma unroll
-            for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w, fv[u][k].get(v), acc[k][v]);
-          }
-        }
-      }
-      m[k] = mx;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) c[u] = cn[u];
+            for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[u][ONE ? 0 : k], fv[u][k].get(v), acc[k][v]);
   }
   // merge the E edge-lane states (fixed xor order)
   for (int off = G; off < L.GE; off <<= 1) {
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const float mo = __shfl_xor_sync(L.group_mask, m[k], off);
-      const float lo = __shfl_xor_sync(L.group_mask, l[k], off);
-      const float mx = fmaxf(m[k], mo);
-      const float a = mx == -INFINITY ? 0.f : __expf(m[k] - mx);
+    for (int j = 0; j < NG; ++j) {
+      const float mo = __shfl_xor_sync(L.group_mask, m[j], off);
+      const float lo = __shfl_xor_sync(L.group_mask, l[j], off);
+      const float mx = fmaxf(m[j], mo);
+      const float a = mx == -INFINITY ? 0.f : __expf(m[j] - mx);
       const float b = mx == -INFINITY ? 0.f : __expf(mo - mx);
-      l[k] = l[k] * a + lo * b;
+      l[j] = l[j] * a + lo * b;
 #pragma unroll
-      for (int v = 0; v < VW; ++v) {
-        const float ao = __shfl_xor_sync(L.group_mask, acc[k][v], off);
-        acc[k][v] = acc[k][v] * a + ao * b;
+      for (int k = 0; k < NV; ++k) {
+        if (!(ONE || k == j)) continue;
+#pragma unroll
+        for (int v = 0; v < VW; ++v) {
+          const float ao = __shfl_xor_sync(L.group_mask, acc[k][v], off);
+          acc[k][v] = acc[k][v] * a + ao * b;
+        }
       }
-      m[k] = mx;
+      m[j] = mx;
     }
   }
   if (!it.active || L.e != 0) return;
@@ -179,22 +208,24 @@ __global__ void __launch_bounds__(kBlock) attention_kernel(
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       if (!valid[k]) continue;
-      const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+      const float lk = l[ONE ? 0 : k];
+      const float inv = lk > 0.f ? 1.f / lk : 0.f;
       float r[VW];
 #pragma unroll
       for (int v = 0; v < VW; ++v) r[v] = acc[k][v] * inv;
-      store_frag<T, VW>(o + (int64_t)(g + k * G) * VW, r);
+      store_frag<T, VW>(o + (int64_t)frag[k] * VW, r);
     }
   } else {
     float *pa = part_acc + (int64_t)it.chunk * nfrag * VW;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       if (!valid[k]) continue;
-      store_partial<VW>(pa + (int64_t)(g + k * G) * VW, acc[k]);
-      if ((g + k * G) % cph == 0) {
-        float *pm = part_ml + ((int64_t)it.chunk * H + head[k]) * 2;
-        __stcg(pm, m[k]);
-        __stcg(pm + 1, l[k]);
+      store_partial<VW>(pa + (int64_t)frag[k] * VW, acc[k]);
+      if (frag[k] % cph == 0) {
+        const int h = H > 1 ? frag[k] / cph : 0;
+        float *pm = part_ml + ((int64_t)it.chunk * H + h) * 2;
+        __stcg(pm, m[ONE ? 0 : k]);
+        __stcg(pm + 1, l[ONE ? 0 : k]);
       }
     }
   }
@@ -246,13 +277,15 @@ cudaError_t attention_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
   const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
   const int64_t grid = chunk_blocks + (n_rows + per_block - 1) / per_block;
   if (grid > 0) {
-#define AUTOSAGE_ATTN(NVV, GIV)                                                                    \
-  attention_kernel<T, VW, NVV, GIV><<<(unsigned)grid, kBlock, 0, s>>>(                           \
-      n_rows, row_ptr, col_idx, Q, K, scores, V, ld, scale, g.H, g.es, g.cph, g.mshift, g.R, g.nfrag, \
-      g.G, g.E, O, cl, chunk_blocks, part_acc, part_ml)
-#define AUTOSAGE_ATTN_NV(NVV)           \
-  if (scores) AUTOSAGE_ATTN(NVV, true); \
-  else AUTOSAGE_ATTN(NVV, false);
+#define AUTOSAGE_ATTN(NVV, GIV, ONEG)                                                               \
+  attention_kernel<T, VW, NVV, GIV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                       \
+      n_rows, row_ptr, col_idx, Q, K, scores, V, ld, scale, g.H, g.es, g.cph, g.R, g.nfrag, g.G,   \
+      g.E, g.fs, g.ks, O, cl, chunk_blocks, part_acc, part_ml)
+#define AUTOSAGE_ATTN_NV(NVV)                     \
+  if (scores) AUTOSAGE_ATTN(NVV, true, true);     \
+  else if (g.one) AUTOSAGE_ATTN(NVV, false, true); \
+  else AUTOSAGE_ATTN(NVV, false, false);
+    if (scores && !g.one) return cudaErrorInvalidValue;
     switch (g.NV) {
       case 1: AUTOSAGE_ATTN_NV(1); break;
       case 2: AUTOSAGE_ATTN_NV(2); break;

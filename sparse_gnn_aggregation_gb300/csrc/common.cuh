@@ -57,21 +57,25 @@ template <typename T, int VW> struct Frag;
 template <> struct Frag<float, 4> {
   float4 r;
   __device__ __forceinline__ void load(const float *p) { r = __ldg(reinterpret_cast<const float4 *>(p)); }
+  __device__ __forceinline__ void zero() { r = make_float4(0.f, 0.f, 0.f, 0.f); }
   __device__ __forceinline__ float get(int i) const { return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w; }
 };
 template <> struct Frag<float, 2> {
   float2 r;
   __device__ __forceinline__ void load(const float *p) { r = __ldg(reinterpret_cast<const float2 *>(p)); }
+  __device__ __forceinline__ void zero() { r = make_float2(0.f, 0.f); }
   __device__ __forceinline__ float get(int i) const { return i == 0 ? r.x : r.y; }
 };
 template <> struct Frag<float, 1> {
   float r;
   __device__ __forceinline__ void load(const float *p) { r = __ldg(p); }
+  __device__ __forceinline__ void zero() { r = 0.f; }
   __device__ __forceinline__ float get(int) const { return r; }
 };
 template <> struct Frag<__nv_bfloat16, 8> {
   uint4 r;
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const uint4 *>(p)); }
+  __device__ __forceinline__ void zero() { r = make_uint4(0u, 0u, 0u, 0u); }
   __device__ __forceinline__ float get(int i) const {
     const uint32_t w = i < 2 ? r.x : i < 4 ? r.y : i < 6 ? r.z : r.w;
     return (i & 1) ? bf16hi(w) : bf16lo(w);
@@ -80,6 +84,7 @@ template <> struct Frag<__nv_bfloat16, 8> {
 template <> struct Frag<__nv_bfloat16, 4> {
   uint2 r;
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const uint2 *>(p)); }
+  __device__ __forceinline__ void zero() { r = make_uint2(0u, 0u); }
   __device__ __forceinline__ float get(int i) const {
     const uint32_t w = i < 2 ? r.x : r.y;
     return (i & 1) ? bf16hi(w) : bf16lo(w);
@@ -88,6 +93,7 @@ template <> struct Frag<__nv_bfloat16, 4> {
 template <> struct Frag<__nv_bfloat16, 2> {
   uint32_t r;
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const unsigned int *>(p)); }
+  __device__ __forceinline__ void zero() { r = 0u; }
   __device__ __forceinline__ float get(int i) const { return (i & 1) ? bf16hi(r) : bf16lo(r); }
 };
 template <> struct Frag<__nv_bfloat16, 1> {
@@ -95,6 +101,7 @@ template <> struct Frag<__nv_bfloat16, 1> {
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
     r = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p)));
   }
+  __device__ __forceinline__ void zero() { r = 0u; }
   __device__ __forceinline__ float get(int) const { return __uint_as_float(r << 16); }
 };
 

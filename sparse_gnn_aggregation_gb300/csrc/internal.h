@@ -25,9 +25,13 @@ struct Geom {
   int G = 1;
   int E = 1;
   int NV = 1;
-  int mshift = 0;  // log2(slots per head group per lane)
   int R = 1;       // lanes in one head reduction
   int es = 1;      // elements between consecutive edges in per-edge arrays (vals, scores)
+  int fs = 1;      // fragment of slot k on lane g: g * fs + k * ks
+  int ks = 1;
+  bool one = true;       // all slots of a lane belong to one head
+  bool batched = false;  // single-head SDDMM: transpose-reduction over G-edge batches
+  bool comp = false;     // SpMM: compensated (Kahan) accumulation for long serial sums
 };
 
 // SpMM over rows (and chunks of cut rows) with per-edge (per-head) weights.

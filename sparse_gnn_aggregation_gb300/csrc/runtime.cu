@@ -57,11 +57,6 @@ int pow2ceil(int64_t x) {
   while (p < x) p <<= 1;
   return p;
 }
-int log2i(int x) {
-  int r = 0;
-  while ((1 << r) < x) ++r;
-  return r;
-}
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 // ---------------------------------------------------------------- validation
@@ -125,26 +120,33 @@ autosage_status choose_geom(DType dt, int H, int64_t D, std::initializer_list<Ma
   // an explicit edge-lane count with automatic feature lanes keeps the group within a warp
   if (G_req <= 0 && E_req > 0 && is_pow2(E_req) && E_req <= 32) g.G = std::min(g.G, 32 / E_req);
   if (!is_pow2(g.G) || g.G > 32) return fail(AUTOSAGE_ERR_INVALID_ARG, "lanes_f must be a power of two <= 32");
-  if (need_head_reduce && H > 1) {
-    if (!is_pow2(g.cph))
-      return fail(AUTOSAGE_ERR_UNSUPPORTED, "multi-head reduction needs D/VW a power of two");
-    // (both powers of two: one divides the other)
-  }
   const int64_t per_lane = (g.nfrag + g.G - 1) / g.G;
   g.NV = pow2ceil(per_lane);
   if (g.NV > nv_max)
     return fail(AUTOSAGE_ERR_UNSUPPORTED, "feature width %" PRId64 " too large for one pass", F);
   g.E = E_req > 0 ? E_req : std::max(1, std::min(32 / g.G, 8));
   if (!is_pow2(g.E) || g.G * g.E > 32) return fail(AUTOSAGE_ERR_INVALID_ARG, "lanes_f * lanes_e must be <= 32");
+  // fragment-to-lane mapping and head reductions
+  g.fs = 1;
+  g.ks = g.G;
+  g.one = true;
+  g.R = g.G;
+  g.batched = false;
   if (H == 1) {
-    g.mshift = log2i(g.NV);
-    g.R = g.G;
-  } else if (g.cph <= g.G) {
-    g.mshift = 0;
-    g.R = g.cph;
-  } else {
-    g.mshift = log2i(g.cph / g.G);
-    g.R = g.G;
+    g.batched = g.G >= 4 && g.G <= 16;  // at 32 lanes the batch of 32 partial dots costs occupancy
+  } else if (need_head_reduce) {
+    if (!is_pow2(g.cph))
+      return fail(AUTOSAGE_ERR_UNSUPPORTED, "multi-head reduction needs D/VW a power of two");
+    if (g.NV <= g.cph) {  // consecutive fragments per lane, all in one head
+      g.fs = g.NV;
+      g.ks = 1;
+      g.R = g.cph / g.NV;
+    } else if (g.cph <= g.G) {  // interleaved lanes, one head per slot
+      g.one = false;
+      g.R = g.cph;
+    } else {
+      return fail(AUTOSAGE_ERR_UNSUPPORTED, "head width does not fit the lane mapping");
+    }
   }
   return AUTOSAGE_OK;
 }
@@ -237,6 +239,8 @@ struct autosage_plan_s {
   double probe_ms = -1;
   double est_ms = -1;
   bool from_cache = false;
+  int64_t maxdeg = -1;  // longest row of the walked CSR (-1: not computed)
+  bool comp = true;     // SpMM: compensated accumulation (serial sums longer than 512 edges)
   // the CSR the kernels walk (A, or A^T for SPMM_T)
   int64_t k_rows = 0;
   const int32_t *k_row_ptr = nullptr;
@@ -383,6 +387,20 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
   P->cl = ChunkList{};
   P->mp_warps = 0;
   autosage_status st = AUTOSAGE_OK;
+  if (P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) {
+    if (P->maxdeg < 0) {
+      RowStats rs;
+      st = gpu_row_stats(P->k_rows, P->k_row_ptr, 1024, rs, s);
+      if (st != AUTOSAGE_OK) return st;
+      P->maxdeg = rs.ints[2];
+    }
+    // longest run of edges one lane sums serially (edge lanes taken as 1 when automatic)
+    const int64_t lanes_e = P->sched.E > 0 ? P->sched.E : 1;
+    int64_t run = P->maxdeg;
+    if (P->sched.kind == AUTOSAGE_SCHED_SPLIT) run = std::min<int64_t>(run, P->sched.split);
+    if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) run = std::min<int64_t>(run, P->sched.split);
+    P->comp = run / lanes_e > 512;
+  }
   if (P->sched.kind == AUTOSAGE_SCHED_SPLIT) {
     st = build_split(P, P->sched.split, s);
   } else if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
@@ -437,6 +455,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
         Geom gt;
         st = choose_geom(P->dt, 1, w, {{x, a.ldx}, {y, a.ldy}}, P->sched.G, E_req, false, 16, gt);
         if (st != AUTOSAGE_OK) return st;
+        gt.comp = P->comp;
         if (mp) {
           gt.E = 32 / gt.G;
           e = launch_spmm_mergepath(gt, P->k_rows, P->k_row_ptr, P->k_col_idx, P->k_vals, x, a.ldx, y,
@@ -463,7 +482,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
     case AUTOSAGE_OP_ATTN: {
       const int64_t ld = P->H * P->F;
       if (a.given) {
-        st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, P->sched.G, P->sched.E, false, 8, g);
+        st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, P->sched.G, P->sched.E, true, 8, g);
       } else {
         st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}, {a.X, ld}, {a.Y, ld}}, P->sched.G,
                          P->sched.E, true, 8, g);

@@ -4,23 +4,47 @@
 // CSR attention pipeline). Edge values of A are not multiplied in.
 //
 // A lane group owns a row (or a chunk of a cut row): its G feature lanes hold
-// the row's Q fragments in registers for the whole row, every edge gathers one
-// K row, and the per-head dot product is finished by xor shuffles among the
-// lanes holding that head. Cut rows need no fix-up: every edge's score is
-// complete within its chunk.
+// the row's Q fragments in registers for the whole row and every edge gathers
+// one K row. Two ways to finish the dot products:
+//  * per edge: the lanes holding a head reduce it with xor shuffles
+//    (log2 R rounds per edge and head);
+//  * batched (single head): each lane keeps its partial dot for G edges and
+//    one transpose-reduction over the G lanes (G - 1 shuffles for G edges)
+//    leaves edge j's total on lane j, which also makes the score writes of a
+//    batch one contiguous store.
+// Cut rows need no fix-up: every edge's score is complete within its chunk.
 #include "internal.h"
 
 namespace autosage {
 
 namespace {
 
-template <typename T, int VW, int NV, int U>
-__device__ __forceinline__ void sddmm_edges(const Lanes &L, const int32_t *__restrict__ col_idx,
-                                            const T *__restrict__ K, int64_t ldk,
-                                            const float (&q)[NV][VW], int nfrag, int H, int es,
-                                            int cph, int mshift, int R, float *__restrict__ S, int p0,
-                                            int pe) {
-  const int G = L.G, E = L.E, g = L.g;
+// Per-edge reduction. Fragment slot k of lane g is fragment g * fs + k * ks.
+// ONE: all slots of a lane belong to one head; otherwise slot k is its own head.
+template <typename T, int VW, int NV, bool ONE>
+__global__ void __launch_bounds__(kBlock) sddmm_kernel(
+    int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
+    const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha,
+    int H, int es, int cph, int R, int nfrag, int G, int E, int fs, int ks, float *__restrict__ S,
+    ChunkList cl, int64_t chunk_blocks) {
+  constexpr int NG = ONE ? 1 : NV;
+  const Lanes L(G, E);
+  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  const int g = L.g;
+  int frag[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) frag[k] = g * fs + k * ks;
+  float q[NV][VW];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    Frag<T, VW> f;
+    const bool ok = it.active && it.e > it.b && frag[k] < nfrag;
+    if (ok) f.load(Q + it.row * ldq + (int64_t)frag[k] * VW);
+#pragma unroll
+    for (int v = 0; v < VW; ++v) q[k][v] = ok ? alpha * f.get(v) : 0.f;
+  }
+  constexpr int U = NV * VW <= 8 ? 4 : (NV * VW <= 16 ? 2 : 1);
+  const int p0 = it.b + L.e, pe = it.e;
   int c[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) c[u] = p0 + u * E < pe ? ld_stream_i32(col_idx + p0 + u * E) : 0;
@@ -33,42 +57,37 @@ __device__ __forceinline__ void sddmm_edges(const Lanes &L, const int32_t *__res
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (live[u] && g + k * G < nfrag) f[u][k].load(K + (int64_t)c[u] * ldk + (int64_t)(g + k * G) * VW);
+        if (live[u] && frag[k] < nfrag) f[u][k].load(K + (int64_t)c[u] * ldk + (int64_t)frag[k] * VW);
     // next iteration's columns are fetched while these rows are in flight
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int q = p + U * E + u * E;
-      c[u] = q < pe ? ld_stream_i32(col_idx + q) : 0;
+      const int qe = p + U * E + u * E;
+      c[u] = qe < pe ? ld_stream_i32(col_idx + qe) : 0;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      // partial dot per fragment slot, summed into head groups of 2^mshift slots
-      float hs[NV];
+      float hs[NG];
 #pragma unroll
-      for (int k = 0; k < NV; ++k) hs[k] = 0.f;
+      for (int j = 0; j < NG; ++j) hs[j] = 0.f;
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
-        if (live[u] && g + k * G < nfrag) {
+        if (live[u] && frag[k] < nfrag) {
           float d = 0.f;
 #pragma unroll
           for (int v = 0; v < VW; ++v) d = fmaf(q[k][v], f[u][k].get(v), d);
-          hs[k >> mshift] += d;
+          hs[ONE ? 0 : k] += d;
         }
       }
       // every lane of this edge lane's G-lane segment runs the same trip count
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        if ((j << mshift) >= NV) break;
+      for (int j = 0; j < NG; ++j)
         for (int off = 1; off < R; off <<= 1) hs[j] += __shfl_xor_sync(L.sub_mask, hs[j], off);
-      }
-      if (live[u]) {
+      if (live[u] && (g % R) == 0) {
         const int64_t pp = p + u * E;
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          if ((j << mshift) >= NV) break;
-          const int c0 = g + (j << mshift) * G;  // first fragment of this head group
-          if (c0 < nfrag && (g % R) == 0) {
-            const int h = H > 1 ? c0 / cph : 0;
+        for (int j = 0; j < NG; ++j) {
+          if (frag[j] < nfrag) {
+            const int h = H > 1 ? frag[j] / cph : 0;
             S[pp * es + h] = hs[j];
           }
         }
@@ -77,25 +96,91 @@ __device__ __forceinline__ void sddmm_edges(const Lanes &L, const int32_t *__res
   }
 }
 
-template <typename T, int VW, int NV>
-__global__ void __launch_bounds__(kBlock) sddmm_kernel(
+// Batched single-head SDDMM: G (compile time) feature lanes per edge lane.
+template <typename T, int VW, int NV, int G>
+__global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
-    const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha,
-    int H, int es, int cph, int mshift, int R, int nfrag, int G, int E, float *__restrict__ S,
-    ChunkList cl, int64_t chunk_blocks) {
+    const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha, int es,
+    int nfrag, int E, float *__restrict__ S, ChunkList cl, int64_t chunk_blocks) {
   const Lanes L(G, E);
   const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  const int g = L.g;
   float q[NV][VW];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     Frag<T, VW> f;
-    const bool ok = it.active && it.e > it.b && L.g + k * G < nfrag;
-    if (ok) f.load(Q + it.row * ldq + (int64_t)(L.g + k * G) * VW);
+    const bool ok = it.active && it.e > it.b && g + k * G < nfrag;
+    if (ok) f.load(Q + it.row * ldq + (int64_t)(g + k * G) * VW);
 #pragma unroll
     for (int v = 0; v < VW; ++v) q[k][v] = ok ? alpha * f.get(v) : 0.f;
   }
-  constexpr int U = NV * VW <= 8 ? 4 : (NV * VW <= 16 ? 2 : 1);
-  sddmm_edges<T, VW, NV, U>(L, col_idx, K, ldk, q, nfrag, H, es, cph, mshift, R, S, it.b + L.e, it.e);
+  // edges of this edge lane: p = it.b + e + E * t; batches of G consecutive t
+  const int first = it.b + L.e;
+  const int n_mine = it.e > first ? (it.e - first + E - 1) / E : 0;
+  const int base_lane = L.slot * L.GE + L.e * G;  // lane 0 of this edge lane's segment
+  constexpr int U = G < 4 ? G : 4;
+  for (int t0 = 0; t0 < n_mine; t0 += G) {
+    const int nb = min(G, n_mine - t0);
+    // one load brings the batch's column indices, lane j holding edge j's
+    const int pj = first + (t0 + g) * E;
+    const int my_col = g < nb ? ld_stream_i32(col_idx + pj) : 0;
+    float part[G];
+#pragma unroll
+    for (int j0 = 0; j0 < G; j0 += U) {
+      Frag<T, VW> f[U][NV];
+      int cj[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) cj[u] = __shfl_sync(L.sub_mask, my_col, base_lane + j0 + u);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (j0 + u < nb && g + k * G < nfrag)
+            f[u][k].load(K + (int64_t)cj[u] * ldk + (int64_t)(g + k * G) * VW);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float d = 0.f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (j0 + u < nb && g + k * G < nfrag)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) d = fmaf(q[k][v], f[u][k].get(v), d);
+        part[j0 + u] = d;
+      }
+    }
+    // transpose-reduce: after the stage on bit s, a lane keeps the half of the
+    // edges whose index has its own bit s, summed with its partner's half
+#pragma unroll
+    for (int sbit = G / 2; sbit >= 1; sbit >>= 1) {
+      const bool upper = (g & sbit) != 0;
+#pragma unroll
+      for (int i = 0; i < sbit; ++i) {
+        const float send = upper ? part[i] : part[i + sbit];
+        const float keep = upper ? part[i + sbit] : part[i];
+        part[i] = keep + __shfl_xor_sync(L.sub_mask, send, sbit);
+      }
+    }
+    if (g < nb) S[(int64_t)pj * es] = part[0];
+  }
+}
+
+template <typename T, int VW, int NV>
+cudaError_t launch_batched(const Geom &g, int64_t grid, int64_t n_rows, const int32_t *row_ptr,
+                           const int32_t *col_idx, const T *Q, int64_t ldq, const T *K, int64_t ldk,
+                           float alpha, float *S, const ChunkList &cl, int64_t chunk_blocks, cudaStream_t s) {
+#define AUTOSAGE_SDDMM_B(GG)                                                                              \
+  sddmm_batched_kernel<T, VW, NV, GG><<<(unsigned)grid, kBlock, 0, s>>>(                                \
+      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.E, S, cl, chunk_blocks)
+  switch (g.G) {
+    case 2: AUTOSAGE_SDDMM_B(2); break;
+    case 4: AUTOSAGE_SDDMM_B(4); break;
+    case 8: AUTOSAGE_SDDMM_B(8); break;
+    case 16: AUTOSAGE_SDDMM_B(16); break;
+    case 32: AUTOSAGE_SDDMM_B(32); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef AUTOSAGE_SDDMM_B
+  return cudaGetLastError();
 }
 
 template <typename T, int VW>
@@ -106,11 +191,23 @@ cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, cons
   const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
   const int64_t grid = chunk_blocks + (n_rows + per_block - 1) / per_block;
   if (grid <= 0) return cudaSuccess;
-#define AUTOSAGE_SDDMM_NV(NVV)                                                                    \
-  sddmm_kernel<T, VW, NVV><<<(unsigned)grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, Q, ldq, K, \
-                                                             ldk, alpha, g.H, g.es, g.cph, g.mshift, \
-                                                             g.R, g.nfrag, g.G, g.E, S, cl,      \
-                                                             chunk_blocks)
+  // batched transpose-reduction: single head, 16-byte fragments, 2..32 lanes
+  if constexpr (sizeof(T) * VW == 16) {
+    if (g.H == 1 && g.batched && g.G >= 2 && g.fs == 1 && g.NV <= 4) {
+      switch (g.NV) {
+        case 1: return launch_batched<T, VW, 1>(g, grid, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, chunk_blocks, s);
+        case 2: return launch_batched<T, VW, 2>(g, grid, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, chunk_blocks, s);
+        case 4: return launch_batched<T, VW, 4>(g, grid, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, chunk_blocks, s);
+      }
+    }
+  }
+#define AUTOSAGE_SDDMM(NVV, ONEG)                                                                     \
+  sddmm_kernel<T, VW, NVV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                                 \
+      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.H, g.es, g.cph, g.R, g.nfrag, g.G, g.E,     \
+      g.fs, g.ks, S, cl, chunk_blocks)
+#define AUTOSAGE_SDDMM_NV(NVV)              \
+  if (g.one) AUTOSAGE_SDDMM(NVV, true);     \
+  else AUTOSAGE_SDDMM(NVV, false);
   switch (g.NV) {
     case 1: AUTOSAGE_SDDMM_NV(1); break;
     case 2: AUTOSAGE_SDDMM_NV(2); break;
@@ -120,6 +217,7 @@ cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, cons
     default: return cudaErrorInvalidValue;
   }
 #undef AUTOSAGE_SDDMM_NV
+#undef AUTOSAGE_SDDMM
   return cudaGetLastError();
 }
 

@@ -26,6 +26,21 @@ __device__ __forceinline__ void zero(float (&acc)[NV][VW]) {
     for (int v = 0; v < VW; ++v) acc[k][v] = 0.f;
 }
 
+// acc += w * x, plain or compensated (Kahan): long rows of signed terms can
+// cancel to a small result whose fp32 rounding error, accumulated over tens of
+// thousands of additions, would otherwise approach the result itself.
+template <bool COMP>
+__device__ __forceinline__ void accum(float &acc, float &comp, float w, float x) {
+  if constexpr (COMP) {
+    const float y = fmaf(w, x, -comp);
+    const float t = acc + y;
+    comp = (t - acc) - y;
+    acc = t;
+  } else {
+    acc = fmaf(w, x, acc);
+  }
+}
+
 // Edge weights of U edges p, p + E, ... for every fragment slot.
 template <int U, int NV>
 __device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx,
@@ -54,12 +69,12 @@ __device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx
 // Full iterations take U edges per edge lane; the next iteration's column
 // indices and weights are loaded while this iteration's rows are in flight,
 // so each iteration waits on one memory round trip, not two.
-template <typename T, int VW, int NV, int U>
+template <typename T, int VW, int NV, int U, bool COMP>
 __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx,
                                              const float *__restrict__ vals, int H, int es,
                                              const int (&head)[NV], const T *__restrict__ X,
                                              int64_t ldx, int nfrag, int g, int G, int E, int p0,
-                                             int pe, float (&acc)[NV][VW]) {
+                                             int pe, float (&acc)[NV][VW], float (&comp)[NV][VW]) {
   int p = p0;
   if constexpr (U > 1) {
     if (p + (U - 1) * E < pe) {
@@ -84,7 +99,7 @@ __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx
           for (int k = 0; k < NV; ++k)
             if (g + k * G < nfrag)
 #pragma unroll
-              for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[u][k], f[u][k].get(v), acc[k][v]);
+              for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[u][k], f[u][k].get(v));
         p = pn;
         if (!more) break;
 #pragma unroll
@@ -112,7 +127,7 @@ __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx
     for (int k = 0; k < NV; ++k)
       if (g + k * G < nfrag)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[k], f[k].get(v), acc[k][v]);
+        for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[k], f[k].get(v));
   }
 }
 
@@ -131,7 +146,7 @@ template <int NV, int VW> constexpr int unroll_for() {
   return NV * VW <= 8 ? 4 : (NV * VW <= 16 ? 2 : 1);
 }
 
-template <typename T, int VW, int NV>
+template <typename T, int VW, int NV, bool COMP>
 __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const float *__restrict__ vals, int H, int es, int cph, const T *__restrict__ X, int64_t ldx,
@@ -145,10 +160,11 @@ __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
     const int c = L.g + k * G;
     head[k] = (H > 1 && c < nfrag) ? c / cph : 0;
   }
-  float acc[NV][VW];
+  float acc[NV][VW], comp[NV][VW];
   zero(acc);
-  gather_edges<T, VW, NV, unroll_for<NV, VW>()>(col_idx, vals, H, es, head, X, ldx, nfrag, L.g, G, E,
-                                                 it.b + L.e, it.e, acc);
+  zero(comp);
+  gather_edges<T, VW, NV, unroll_for<NV, VW>(), COMP>(col_idx, vals, H, es, head, X, ldx, nfrag, L.g, G, E,
+                                                       it.b + L.e, it.e, acc, comp);
   reduce_edge_lanes(acc, L.group_mask, G, L.GE);
   if (!it.active || L.e != 0) return;
   if (it.chunk < 0) {
@@ -179,10 +195,13 @@ __global__ void __launch_bounds__(kBlock) spmm_fixup_kernel(ChunkList cl, int nf
     float acc[VW];
 #pragma unroll
     for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+    float comp[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) comp[v] = 0.f;
     for (int c = c0; c < c1; ++c) {
       const float *src = partial + (int64_t)c * F + (int64_t)f * VW;
 #pragma unroll
-      for (int v = 0; v < VW; ++v) acc[v] += __ldcg(src + v);
+      for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, __ldcg(src + v));
     }
     store_frag<T, VW>(Y + row * ldy + (int64_t)f * VW, acc);
   }
@@ -216,7 +235,7 @@ __global__ void mergepath_partition_kernel(int64_t n_rows, int64_t nnz,
   part[w] = merge_path_search(d, n_rows, nnz, row_ptr);
 }
 
-template <typename T, int VW, int NV>
+template <typename T, int VW, int NV, bool COMP>
 __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const float *__restrict__ vals, const T *__restrict__ X, int64_t ldx, T *__restrict__ Y,
@@ -230,9 +249,10 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
   constexpr int U = unroll_for<NV, VW>();
   for (int i = s0.x; i < s1.x; ++i) {
     const int b = max(row_ptr[i], s0.y), e = row_ptr[i + 1];
-    float acc[NV][VW];
+    float acc[NV][VW], comp[NV][VW];
     zero(acc);
-    gather_edges<T, VW, NV, U>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, e, acc);
+    zero(comp);
+    gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, e, acc, comp);
     reduce_edge_lanes(acc, FULL, G, 32);
     if (L.e == 0) {
       T *y = Y + (int64_t)i * ldy;
@@ -247,9 +267,11 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
     const int b = max(row_ptr[s1.x], s0.y);
     if (s1.y > b) {
       crow = s1.x;
-      float acc[NV][VW];
+      float acc[NV][VW], comp[NV][VW];
       zero(acc);
-      gather_edges<T, VW, NV, U>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, s1.y, acc);
+      zero(comp);
+      gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, s1.y, acc,
+                                       comp);
       reduce_edge_lanes(acc, FULL, G, 32);
       if (L.e == 0) {
         float *cv = carry_val + w * (int64_t)nfrag * VW;
@@ -278,10 +300,13 @@ __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
     float acc[VW];
 #pragma unroll
     for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+    float comp[VW];
+#pragma unroll
+    for (int v = 0; v < VW; ++v) comp[v] = 0.f;
     for (int64_t q = w; q < n_warps && carry_row[q] == r; ++q) {
       const float *src = carry_val + q * F + (int64_t)f * VW;
 #pragma unroll
-      for (int v = 0; v < VW; ++v) acc[v] += __ldcg(src + v);
+      for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, __ldcg(src + v));
     }
     T *y = Y + (int64_t)r * ldy + (int64_t)f * VW;
     Frag<T, VW> cur;
@@ -303,10 +328,13 @@ cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const
   const int64_t row_blocks = (n_rows + per_block - 1) / per_block;
   const int64_t grid = chunk_blocks + row_blocks;
   if (grid > 0) {
-#define AUTOSAGE_SPMM_NV(NVV)                                                                     \
-  spmm_rows_kernel<T, VW, NVV><<<(unsigned)grid, kBlock, 0, s>>>(                               \
+#define AUTOSAGE_SPMM_K(NVV, CMP)                                                                 \
+  spmm_rows_kernel<T, VW, NVV, CMP><<<(unsigned)grid, kBlock, 0, s>>>(                          \
       n_rows, row_ptr, col_idx, vals, g.H, g.es, g.cph, X, ldx, Y, ldy, g.nfrag, g.G, g.E, cl,    \
       chunk_blocks, partial)
+#define AUTOSAGE_SPMM_NV(NVV)          \
+  if (g.comp) AUTOSAGE_SPMM_K(NVV, true); \
+  else AUTOSAGE_SPMM_K(NVV, false);
     switch (g.NV) {
       case 1: AUTOSAGE_SPMM_NV(1); break;
       case 2: AUTOSAGE_SPMM_NV(2); break;
@@ -316,6 +344,7 @@ cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const
       default: return cudaErrorInvalidValue;
     }
 #undef AUTOSAGE_SPMM_NV
+#undef AUTOSAGE_SPMM_K
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -334,10 +363,13 @@ cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          int32_t *carry_row, cudaStream_t s) {
   if (n_warps <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_warps + kBlock / 32 - 1) / (kBlock / 32));
-#define AUTOSAGE_MP_NV(NVV)                                                                         \
-  spmm_mergepath_kernel<T, VW, NVV><<<grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, vals, X, ldx, \
-                                                           Y, ldy, g.nfrag, g.G, g.E, part,        \
-                                                           n_warps, carry_val, carry_row)
+#define AUTOSAGE_MP_K(NVV, CMP)                                                                    \
+  spmm_mergepath_kernel<T, VW, NVV, CMP><<<grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, vals, X,  \
+                                                                ldx, Y, ldy, g.nfrag, g.G, g.E,     \
+                                                                part, n_warps, carry_val, carry_row)
+#define AUTOSAGE_MP_NV(NVV)           \
+  if (g.comp) AUTOSAGE_MP_K(NVV, true); \
+  else AUTOSAGE_MP_K(NVV, false);
   switch (g.NV) {
     case 1: AUTOSAGE_MP_NV(1); break;
     case 2: AUTOSAGE_MP_NV(2); break;
@@ -347,6 +379,7 @@ cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
     default: return cudaErrorInvalidValue;
   }
 #undef AUTOSAGE_MP_NV
+#undef AUTOSAGE_MP_K
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   mergepath_fixup_kernel<T, VW><<<grid, kBlock, 0, s>>>(n_warps, g.nfrag, carry_val, carry_row, Y, ldy);

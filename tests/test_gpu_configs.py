@@ -1,0 +1,144 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark uses (schedules from the planner with probes), on sampled rows the
+oracle computes one by one: the highest-degree rows, the first and last rows
+and an even spread of the rest.
+
+Workloads (synthetic stand-ins, seeded): R-MAT scale 20 and its uniform
+control; a lognormal power-law graph shaped like OGBN-Products (2,449,029
+nodes, 123.7M edges, mean aggregation); a 50-community power-law graph
+shaped like Reddit (232,965 nodes, 114.6M edges); multi-head bf16 attention
+on R-MAT scale 20.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TOL_BF16, TOL_F32, assert_close, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import sparse_gnn_aggregation_gb300 as sga  # noqa: E402
+
+FLAGS = sga.PLAN_PROBE | sga.PLAN_VERIFY
+
+
+def sample_rows(g, n=1500, top=40):
+    deg = g.degrees()
+    hub = np.argsort(deg, kind="stable")[-top:]
+    spread = np.linspace(0, g.n_rows - 1, n).astype(np.int64)
+    return np.unique(np.concatenate([hub, spread, [0, g.n_rows - 1]]))
+
+
+def mat(g):
+    return sga.CsrMatrix.from_numpy(g.row_ptr, g.col_idx, g.vals, g.n_cols)
+
+
+def edge_index(g, rows):
+    return np.concatenate([np.arange(g.row_ptr[r], g.row_ptr[r + 1]) for r in rows])
+
+
+@pytest.fixture(scope="module")
+def rmat20():
+    return synth.rmat_skew(20, seed=0)
+
+
+@pytest.fixture(scope="module")
+def control(rmat20):
+    return synth.uniform_control(rmat20, seed=0)
+
+
+def check_spmm(g, F, transpose=False, seed=0):
+    A = mat(g)
+    src = g.n_rows if transpose else g.n_cols
+    X = synth.normal(src, F, seed, synth.STREAM_X)
+    plan = sga.autosage_plan(A, sga.OP_SPMM_T if transpose else sga.OP_SPMM, F, flags=FLAGS)
+    Y = sga.autosage_spmm(A, torch.from_numpy(X).cuda(), transpose=transpose, plan=plan)
+    if transpose:
+        rpt, cit, vt = oracle.transpose(g.row_ptr, g.col_idx, g.vals, g.n_cols)
+        gt = synth.Csr(g.n_cols, g.n_rows, rpt, cit, vt)
+        rows = sample_rows(gt)
+        ref = oracle.spmm(rpt, cit, vt, X, rows=rows)
+    else:
+        rows = sample_rows(g)
+        ref = oracle.spmm(g.row_ptr, g.col_idx, g.vals, X, rows=rows)
+    got = Y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_close(got, ref, TOL_F32, f"spmm F={F} T={transpose} [{plan.describe()}]")
+
+
+def check_sddmm(g, F, seed=0):
+    A = mat(g)
+    Q = synth.normal(g.n_rows, F, seed, synth.STREAM_Q)
+    K = synth.normal(g.n_cols, F, seed, synth.STREAM_K)
+    plan = sga.autosage_plan(A, sga.OP_SDDMM, F, flags=FLAGS)
+    S = sga.autosage_sddmm(A, torch.from_numpy(Q).cuda(), torch.from_numpy(K).cuda(), 1.0, plan=plan)
+    rows = sample_rows(g)
+    ref = oracle.sddmm(g.row_ptr, g.col_idx, Q, K, 1.0, rows=rows)[:, 0]
+    got = S[torch.from_numpy(edge_index(g, rows)).cuda()].cpu().numpy()
+    assert_close(got, ref, TOL_F32, f"sddmm F={F} [{plan.describe()}]")
+
+
+@pytest.mark.parametrize("F", [4, 16, 64, 256])
+def test_rmat20_spmm(rmat20, F):
+    check_spmm(rmat20, F)
+
+
+@pytest.mark.parametrize("F", [4, 64, 256])
+def test_rmat20_sddmm(rmat20, F):
+    check_sddmm(rmat20, F)
+
+
+@pytest.mark.parametrize("F", [8, 128])
+def test_control_spmm_sddmm(control, F):
+    check_spmm(control, F)
+    check_sddmm(control, F)
+
+
+def test_rmat20_spmm_transpose(rmat20):
+    check_spmm(rmat20, 64, transpose=True)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_rmat20_attention_bf16(rmat20, fused):
+    g = rmat20
+    A = mat(g)
+    H, D = 8, 64
+    Qb, Q32 = bf16_tensor(synth.normal(g.n_rows, H * D, 0, synth.STREAM_Q))
+    Kb, K32 = bf16_tensor(synth.normal(g.n_cols, H * D, 0, synth.STREAM_K))
+    Vb, V32 = bf16_tensor(synth.normal(g.n_cols, H * D, 0, synth.STREAM_V))
+    plan = sga.autosage_plan(A, sga.OP_ATTN if fused else sga.OP_ATTN_UNFUSED, D, heads=H,
+                             dtype=torch.bfloat16, flags=FLAGS)
+    O = sga.autosage_csr_attention(A, Qb, Kb, Vb, H, 0.125, fused=fused, plan=plan)
+    rows = sample_rows(g, n=600)
+    ref = oracle.csr_attention(g.row_ptr, g.col_idx, Q32, K32, V32, H, 0.125, rows=rows)
+    got = O[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert_close(got, ref, TOL_BF16, f"attention fused={fused} [{plan.describe()}]")
+
+
+@pytest.fixture(scope="module")
+def products():
+    return synth.products_like(seed=0)
+
+
+@pytest.mark.parametrize("F", [32, 100])
+def test_products_spmm_forward_and_transpose(products, F):
+    check_spmm(products, F)
+    check_spmm(products, F, transpose=True, seed=1)
+
+
+@pytest.fixture(scope="module")
+def reddit():
+    return synth.reddit_like(seed=0)
+
+
+@pytest.mark.parametrize("F", [128, 602])
+def test_reddit_spmm(reddit, F):
+    check_spmm(reddit, F)
+
+
+def test_reddit_sddmm(reddit):
+    check_sddmm(reddit, 128)
