@@ -47,11 +47,15 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, const T *__restrict__ K, const float *__restrict__ scores,
     const T *__restrict__ V, int64_t ld, float scale, int H, int es, int cph, int R, int nfrag,
-    int G, int E, int fs, int ks, T *__restrict__ O, ChunkList cl, int64_t chunk_blocks,
+    int G, int E, int fs, int ks, T *__restrict__ O, ChunkList cl, int ipb,
     float *__restrict__ part_acc, float *__restrict__ part_ml) {
   constexpr int NG = ONE ? 1 : NV;  // head groups per lane
   const Lanes L(G, E);
-  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+  const Item it = item_at(idx, n_rows, row_ptr, cl);
   const int g = L.g;
   bool valid[NV];
   int frag[NV];
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
       m[j] = mx;
     }
   }
-  if (!it.active || L.e != 0) return;
+  if (!it.active || L.e != 0) continue;
   if (it.chunk < 0) {
     T *o = O + it.row * ld;
 #pragma unroll
@@ -228,6 +232,7 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
         __stcg(pm + 1, l[ONE ? 0 : k]);
       }
     }
+  }
   }
 }
 
@@ -273,14 +278,13 @@ cudaError_t attention_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const T *Q, const T *K, const float *scores,
                          const T *V, int64_t ld, float scale, T *O, const ChunkList &cl,
                          float *part_acc, float *part_ml, cudaStream_t s) {
-  const int64_t per_block = (kBlock / 32) * (32 / (g.G * g.E));
-  const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
-  const int64_t grid = chunk_blocks + (n_rows + per_block - 1) / per_block;
+  const int ipb = items_per_block_for(g.G * g.E);
+  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
 #define AUTOSAGE_ATTN(NVV, GIV, ONEG)                                                               \
   attention_kernel<T, VW, NVV, GIV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                       \
-      n_rows, row_ptr, col_idx, Q, K, scores, V, ld, scale, g.H, g.es, g.cph, g.R, g.nfrag, g.G,   \
-      g.E, g.fs, g.ks, O, cl, chunk_blocks, part_acc, part_ml)
+      n_rows, row_ptr, col_idx, Q, K, scores, V, ld, scale, g.H, g.es, g.cph, g.R, g.nfrag, g.G,     \
+      g.E, g.fs, g.ks, O, cl, ipb, part_acc, part_ml)
 #define AUTOSAGE_ATTN_NV(NVV)                     \
   if (scores) AUTOSAGE_ATTN(NVV, true, true);     \
   else if (g.one) AUTOSAGE_ATTN(NVV, false, true); \

@@ -152,43 +152,68 @@ struct ChunkList {
   int split = 0;  // 0: no row is cut
 };
 
-// Resolve the work item of a group: blocks [0, chunk_blocks) take chunks,
-// the rest take rows. Returns false (b == e) for idle groups and for rows
-// handled through chunks; such groups still take part in group shuffles.
+// One work item: (row, edge begin, edge end, chunk slot or -1 for a whole row).
+// Inactive items (b == e) still take part in their group's shuffles.
 struct Item {
   int64_t row;
   int b, e;
-  int chunk;  // -1 for a whole row
+  int chunk;
   bool active;
 };
 
-__device__ __forceinline__ Item resolve_item(const Lanes &L, int64_t n_rows, const int32_t *row_ptr,
-                                             const ChunkList &cl, int64_t chunk_blocks) {
+// Work item number idx of a persistent launch: the chunks of cut rows come
+// first (the longest items start earliest), then every row in order.
+__device__ __forceinline__ Item item_at(int64_t idx, int64_t n_rows, const int32_t *row_ptr,
+                                        const ChunkList &cl) {
   Item it{0, 0, 0, -1, false};
-  const int64_t bid = blockIdx.x;
-  if (bid < chunk_blocks) {
-    const int64_t c = L.group_index(bid * (kBlock / 32)) ;
-    if (c < cl.n_chunks) {
-      it.chunk = static_cast<int>(c);
-      it.row = cl.chunk_row[c];
-      it.b = cl.chunk_begin[c];
-      const int re = row_ptr[it.row + 1];
-      it.e = (re - it.b > cl.split) ? it.b + cl.split : re;
-      it.active = true;
-    }
-  } else {
-    const int64_t r = L.group_index((bid - chunk_blocks) * (kBlock / 32));
-    if (r < n_rows) {
-      it.row = r;
-      it.b = row_ptr[r];
-      it.e = row_ptr[r + 1];
-      it.active = !(cl.split > 0 && it.e - it.b > cl.split);
-      if (!it.active) it.e = it.b;
-    }
+  if (idx < cl.n_chunks) {
+    it.chunk = static_cast<int>(idx);
+    it.row = cl.chunk_row[idx];
+    it.b = cl.chunk_begin[idx];
+    const int re = row_ptr[it.row + 1];
+    it.e = (re - it.b > cl.split) ? it.b + cl.split : re;
+    it.active = true;
+  } else if (idx - cl.n_chunks < n_rows) {
+    const int64_t r = idx - cl.n_chunks;
+    it.row = r;
+    it.b = row_ptr[r];
+    it.e = row_ptr[r + 1];
+    it.active = !(cl.split > 0 && it.e - it.b > cl.split);
+    if (!it.active) it.e = it.b;
   }
   return it;
 }
 
+// Items of a launch are dealt to blocks in runs of `ipb`; inside a block the
+// lane groups take the block's items one at a time from a shared counter, so
+// a group that drew short rows goes on with the next item instead of idling
+// until the block's longest row ends. Groups of one warp may take different
+// numbers of items; all their shuffles use group or sub-group masks.
+struct ItemQueue {
+  int64_t base, end;
+  int *counter;
+  __device__ __forceinline__ ItemQueue(int64_t n_rows, const ChunkList &cl, int ipb, int *shared_counter) {
+    base = (int64_t)blockIdx.x * ipb;
+    const int64_t n_items = n_rows + cl.n_chunks;
+    end = base + ipb < n_items ? base + ipb : n_items;
+    counter = shared_counter;
+    if (threadIdx.x == 0) *counter = 0;
+    __syncthreads();
+  }
+  __device__ __forceinline__ bool next(const Lanes &L, int64_t &idx) const {
+    int local = 0;
+    if (L.g == 0 && L.e == 0) local = atomicAdd(counter, 1);
+    local = __shfl_sync(L.group_mask, local, L.slot * L.GE);
+    idx = base + local;
+    return idx < end;
+  }
+};
+
+// Items per block: a few per lane group, so blocks stay short enough for the
+// block scheduler to balance them across SMs.
+inline int items_per_block_for(int GE) { return (kBlock / 32) * (32 / GE) * 4; }
+
 __device__ __forceinline__ int64_t items_per_block(int GE) { return (kBlock / 32) * (32 / GE); }
+
 
 }  // namespace autosage

@@ -26,10 +26,14 @@ __global__ void __launch_bounds__(kBlock) sddmm_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha,
     int H, int es, int cph, int R, int nfrag, int G, int E, int fs, int ks, float *__restrict__ S,
-    ChunkList cl, int64_t chunk_blocks) {
+    ChunkList cl, int ipb) {
   constexpr int NG = ONE ? 1 : NV;
   const Lanes L(G, E);
-  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+  const Item it = item_at(idx, n_rows, row_ptr, cl);
   const int g = L.g;
   int frag[NV];
 #pragma unroll
@@ -94,6 +98,7 @@ __global__ void __launch_bounds__(kBlock) sddmm_kernel(
       }
     }
   }
+  }
 }
 
 // Batched single-head SDDMM: G (compile time) feature lanes per edge lane.
@@ -101,9 +106,13 @@ template <typename T, int VW, int NV, int G>
 __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha, int es,
-    int nfrag, int E, float *__restrict__ S, ChunkList cl, int64_t chunk_blocks) {
+    int nfrag, int E, float *__restrict__ S, ChunkList cl, int ipb) {
   const Lanes L(G, E);
-  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+  const Item it = item_at(idx, n_rows, row_ptr, cl);
   const int g = L.g;
   float q[NV][VW];
 #pragma unroll
@@ -162,15 +171,16 @@ __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
     }
     if (g < nb) S[(int64_t)pj * es] = part[0];
   }
+  }
 }
 
 template <typename T, int VW, int NV>
-cudaError_t launch_batched(const Geom &g, int64_t grid, int64_t n_rows, const int32_t *row_ptr,
+cudaError_t launch_batched(const Geom &g, int64_t grid, int ipb, int64_t n_rows, const int32_t *row_ptr,
                            const int32_t *col_idx, const T *Q, int64_t ldq, const T *K, int64_t ldk,
-                           float alpha, float *S, const ChunkList &cl, int64_t chunk_blocks, cudaStream_t s) {
+                           float alpha, float *S, const ChunkList &cl, cudaStream_t s) {
 #define AUTOSAGE_SDDMM_B(GG)                                                                              \
-  sddmm_batched_kernel<T, VW, NV, GG><<<(unsigned)grid, kBlock, 0, s>>>(                                \
-      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.E, S, cl, chunk_blocks)
+  sddmm_batched_kernel<T, VW, NV, GG><<<(unsigned)grid, kBlock, 0, s>>>(                           \
+      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.E, S, cl, ipb)
   switch (g.G) {
     case 2: AUTOSAGE_SDDMM_B(2); break;
     case 4: AUTOSAGE_SDDMM_B(4); break;
@@ -187,24 +197,23 @@ template <typename T, int VW>
 cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
                      const T *Q, int64_t ldq, const T *K, int64_t ldk, float alpha, float *S,
                      const ChunkList &cl, cudaStream_t s) {
-  const int64_t per_block = (kBlock / 32) * (32 / (g.G * g.E));
-  const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
-  const int64_t grid = chunk_blocks + (n_rows + per_block - 1) / per_block;
+  const int ipb = items_per_block_for(g.G * g.E);
+  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid <= 0) return cudaSuccess;
   // batched transpose-reduction: single head, 16-byte fragments, 2..32 lanes
   if constexpr (sizeof(T) * VW == 16) {
     if (g.H == 1 && g.batched && g.G >= 2 && g.fs == 1 && g.NV <= 4) {
       switch (g.NV) {
-        case 1: return launch_batched<T, VW, 1>(g, grid, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, chunk_blocks, s);
-        case 2: return launch_batched<T, VW, 2>(g, grid, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, chunk_blocks, s);
-        case 4: return launch_batched<T, VW, 4>(g, grid, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, chunk_blocks, s);
+        case 1: return launch_batched<T, VW, 1>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, s);
+        case 2: return launch_batched<T, VW, 2>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, s);
+        case 4: return launch_batched<T, VW, 4>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, s);
       }
     }
   }
 #define AUTOSAGE_SDDMM(NVV, ONEG)                                                                     \
   sddmm_kernel<T, VW, NVV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                                 \
       n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.H, g.es, g.cph, g.R, g.nfrag, g.G, g.E,     \
-      g.fs, g.ks, S, cl, chunk_blocks)
+      g.fs, g.ks, S, cl, ipb)
 #define AUTOSAGE_SDDMM_NV(NVV)              \
   if (g.one) AUTOSAGE_SDDMM(NVV, true);     \
   else AUTOSAGE_SDDMM(NVV, false);

@@ -39,10 +39,14 @@ __device__ __forceinline__ ML ml_merge(ML a, ML b) {
 __global__ void __launch_bounds__(kBlock) softmax_rows_kernel(int64_t n_rows,
                                                               const int32_t *__restrict__ row_ptr,
                                                               int H, int GS, float *__restrict__ S,
-                                                              ChunkList cl, int64_t chunk_blocks,
+                                                              ChunkList cl, int ipb,
                                                               float *__restrict__ ml_out) {
   const Lanes L(GS, 1);
-  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+  const Item it = item_at(idx, n_rows, row_ptr, cl);
   const int64_t i0 = (int64_t)it.b * H, i1 = (int64_t)it.e * H;
   ML a{-INFINITY, 0.f};
   for (int64_t i = i0 + L.g; i < i1; i += GS) ml_add(a, S[i]);
@@ -50,25 +54,30 @@ __global__ void __launch_bounds__(kBlock) softmax_rows_kernel(int64_t n_rows,
     ML b{__shfl_xor_sync(L.group_mask, a.m, off), __shfl_xor_sync(L.group_mask, a.l, off)};
     a = ml_merge(a, b);
   }
-  if (!it.active) return;
+  if (!it.active) continue;
   if (it.chunk >= 0) {
     if (L.g < H) {
       float *o = ml_out + ((int64_t)it.chunk * H + L.g) * 2;
       o[0] = a.m;
       o[1] = a.l;
     }
-    return;
+    continue;
   }
   const float inv = a.l > 0.f ? 1.f / a.l : 0.f;
   for (int64_t i = i0 + L.g; i < i1; i += GS) S[i] = __expf(S[i] - a.m) * inv;
+  }
 }
 
 // Generic head count: one group per row, heads handled one after another.
 __global__ void __launch_bounds__(kBlock) softmax_rows_generic_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, int H, int GS, float *__restrict__ S,
-    ChunkList cl, int64_t chunk_blocks, float *__restrict__ ml_out) {
+    ChunkList cl, int ipb, float *__restrict__ ml_out) {
   const Lanes L(GS, 1);
-  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+  const Item it = item_at(idx, n_rows, row_ptr, cl);
   for (int h = 0; h < H; ++h) {
     ML a{-INFINITY, 0.f};
     for (int64_t p = it.b + L.g; p < it.e; p += GS) ml_add(a, S[p * H + h]);
@@ -87,6 +96,7 @@ __global__ void __launch_bounds__(kBlock) softmax_rows_generic_kernel(
     }
     const float inv = a.l > 0.f ? 1.f / a.l : 0.f;
     for (int64_t p = it.b + L.g; p < it.e; p += GS) S[p * H + h] = __expf(S[p * H + h] - a.m) * inv;
+  }
   }
 }
 
@@ -142,16 +152,13 @@ cudaError_t launch_row_softmax(int64_t n_rows, const int32_t *row_ptr, int H, fl
   if (divides) {
     GS = H < 8 ? 8 : H;
   }
-  const int64_t per_block = (kBlock / 32) * (32 / GS);
-  const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
-  const int64_t grid = chunk_blocks + (n_rows + per_block - 1) / per_block;
+  const int ipb = items_per_block_for(GS);
+  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
     if (divides)
-      softmax_rows_kernel<<<(unsigned)grid, kBlock, 0, s>>>(n_rows, row_ptr, H, GS, S, cl,
-                                                             chunk_blocks, ml);
+      softmax_rows_kernel<<<(unsigned)grid, kBlock, 0, s>>>(n_rows, row_ptr, H, GS, S, cl, ipb, ml);
     else
-      softmax_rows_generic_kernel<<<(unsigned)grid, kBlock, 0, s>>>(n_rows, row_ptr, H, GS, S, cl,
-                                                                     chunk_blocks, ml);
+      softmax_rows_generic_kernel<<<(unsigned)grid, kBlock, 0, s>>>(n_rows, row_ptr, H, GS, S, cl, ipb, ml);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

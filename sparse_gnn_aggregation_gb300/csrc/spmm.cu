@@ -150,33 +150,38 @@ template <typename T, int VW, int NV, bool COMP>
 __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const float *__restrict__ vals, int H, int es, int cph, const T *__restrict__ X, int64_t ldx,
-    T *__restrict__ Y, int64_t ldy, int nfrag, int G, int E, ChunkList cl, int64_t chunk_blocks,
+    T *__restrict__ Y, int64_t ldy, int nfrag, int G, int E, ChunkList cl, int ipb,
     float *__restrict__ partial) {
   const Lanes L(G, E);
-  const Item it = resolve_item(L, n_rows, row_ptr, cl, chunk_blocks);
   int head[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int c = L.g + k * G;
     head[k] = (H > 1 && c < nfrag) ? c / cph : 0;
   }
-  float acc[NV][VW], comp[NV][VW];
-  zero(acc);
-  zero(comp);
-  gather_edges<T, VW, NV, unroll_for<NV, VW>(), COMP>(col_idx, vals, H, es, head, X, ldx, nfrag, L.g, G, E,
-                                                       it.b + L.e, it.e, acc, comp);
-  reduce_edge_lanes(acc, L.group_mask, G, L.GE);
-  if (!it.active || L.e != 0) return;
-  if (it.chunk < 0) {
-    T *y = Y + it.row * ldy;
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+    const Item it = item_at(idx, n_rows, row_ptr, cl);
+    float acc[NV][VW], comp[NV][VW];
+    zero(acc);
+    zero(comp);
+    gather_edges<T, VW, NV, unroll_for<NV, VW>(), COMP>(col_idx, vals, H, es, head, X, ldx, nfrag, L.g, G,
+                                                         E, it.b + L.e, it.e, acc, comp);
+    reduce_edge_lanes(acc, L.group_mask, G, L.GE);
+    if (!it.active || L.e != 0) continue;
+    if (it.chunk < 0) {
+      T *y = Y + it.row * ldy;
 #pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (L.g + k * G < nfrag) store_frag<T, VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
-  } else {
-    float *y = partial + (int64_t)it.chunk * nfrag * VW;
+      for (int k = 0; k < NV; ++k)
+        if (L.g + k * G < nfrag) store_frag<T, VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+    } else {
+      float *y = partial + (int64_t)it.chunk * nfrag * VW;
 #pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (L.g + k * G < nfrag) store_partial<VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+      for (int k = 0; k < NV; ++k)
+        if (L.g + k * G < nfrag) store_partial<VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+    }
   }
 }
 
@@ -323,15 +328,13 @@ template <typename T, int VW>
 cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
                     const float *vals, const T *X, int64_t ldx, T *Y, int64_t ldy,
                     const ChunkList &cl, float *partial, cudaStream_t s) {
-  const int64_t per_block = (kBlock / 32) * (32 / (g.G * g.E));
-  const int64_t chunk_blocks = (cl.n_chunks + per_block - 1) / per_block;
-  const int64_t row_blocks = (n_rows + per_block - 1) / per_block;
-  const int64_t grid = chunk_blocks + row_blocks;
+  const int ipb = items_per_block_for(g.G * g.E);
+  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
 #define AUTOSAGE_SPMM_K(NVV, CMP)                                                                 \
   spmm_rows_kernel<T, VW, NVV, CMP><<<(unsigned)grid, kBlock, 0, s>>>(                          \
-      n_rows, row_ptr, col_idx, vals, g.H, g.es, g.cph, X, ldx, Y, ldy, g.nfrag, g.G, g.E, cl,    \
-      chunk_blocks, partial)
+      n_rows, row_ptr, col_idx, vals, g.H, g.es, g.cph, X, ldx, Y, ldy, g.nfrag, g.G, g.E, cl, ipb, \
+      partial)
 #define AUTOSAGE_SPMM_NV(NVV)          \
   if (g.comp) AUTOSAGE_SPMM_K(NVV, true); \
   else AUTOSAGE_SPMM_K(NVV, false);
