@@ -186,6 +186,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- ranks
+
+def aggregate_ranks(step_ms, step_bytes, world, device="cpu"):
+    """Whole-job rate: every rank ran its own step (weak scaling, no data
+    exchange); the job's step time is the slowest rank's, and the job moved
+    world x step_bytes in it. Returns (max step ms, GB/s)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(step_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    return step_ms, step_bytes * world / (step_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def run_ours(args):
@@ -301,12 +316,7 @@ def run_ours(args):
         tot_bytes += b
         tot_flops += fl
         tot_nnzF += g.nnz * width
-    step_ms = tot_ms
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = tot_bytes * world / (step_ms * 1e-3) / 1e9
+    step_ms, value = aggregate_ranks(tot_ms, tot_bytes, world, dev)
 
     # dominant operation: the largest share of the step
     dom_key = max(per_op, key=lambda k: per_op[k]["ms"])
@@ -405,43 +415,45 @@ def run_ours(args):
 def cpu_baseline(graphs, budget_s=15.0, steps=1):
     """The oracle on the host cores over a row sample of the same operations.
 
-    Rows are sampled evenly (every k-th row) so the sample keeps the degree
-    mix; k is chosen from a calibration run so one pass takes ~budget_s.
-    Value = algorithmic bytes of the sampled rows / oracle time (GB/s).
+    A seeded uniform sample of rows (fraction f of every graph) keeps the
+    degree mix; f is chosen from a calibration pass so one pass takes about
+    budget_s. Value = algorithmic bytes of the sampled rows / oracle time (GB/s).
     """
     import oracle
 
     oracle.build()
     ops = op_list(graphs)
-    rng = np.random.default_rng(0)
-    # features for the sampled rows are drawn once (not timed)
     feats = {}
+    samples = {}
 
-    def sample(g, stride):
-        rows = np.arange(0, g.n_rows, stride, dtype=np.int64)
-        deg = (g.row_ptr[rows + 1] - g.row_ptr[rows]).astype(np.int64)
-        return rows, int(deg.sum())
+    def sample(g, frac):
+        key = (id(g), frac)
+        if key not in samples:
+            rng = np.random.default_rng(12345)
+            k = max(1, min(g.n_rows, int(round(g.n_rows * frac))))
+            rows = np.sort(rng.choice(g.n_rows, size=k, replace=False)).astype(np.int64)
+            deg = (g.row_ptr[rows + 1] - g.row_ptr[rows]).astype(np.int64)
+            samples[key] = (rows, int(deg.sum()))
+        return samples[key]
 
-    def one_pass(stride, timed=True):
+    def one_pass(frac):
         tot_b, tot_t = 0.0, 0.0
         for key, kind, gname, F in ops:
             g = graphs[gname]
-            rows, enn = sample(g, stride)
+            rows, enn = sample(g, frac)
             if key not in feats:
                 W = F * (HEADS if kind.startswith("attn") else 1)
-                feats[key] = rng.standard_normal((g.n_cols, W), dtype=np.float32)
+                feats[key] = np.random.default_rng(1).standard_normal((g.n_cols, W), dtype=np.float32)
             X = feats[key]
+            if kind == "spmm_t" and "T" not in feats:
+                feats["T"] = oracle.transpose(g.row_ptr, g.col_idx, g.vals, g.n_cols)
             t0 = time.perf_counter()
-            if kind in ("spmm", "spmm_t"):
-                # A^T rows are sampled from the transposed CSR built once outside timing
-                if kind == "spmm_t":
-                    if "T" not in feats:
-                        feats["T"] = oracle.transpose(g.row_ptr, g.col_idx, g.vals, g.n_cols)
-                    rpt, cit, vt = feats["T"]
-                    t0 = time.perf_counter()
-                    oracle.spmm(rpt, cit, vt, X, rows=rows)
-                else:
-                    oracle.spmm(g.row_ptr, g.col_idx, g.vals, X, rows=rows)
+            if kind == "spmm_t":
+                rpt, cit, vt = feats["T"]
+                oracle.spmm(rpt, cit, vt, X, rows=rows)
+                b = 4 * (rows.size + 1) + 8 * enn + enn * F * 4 + rows.size * F * 4
+            elif kind == "spmm":
+                oracle.spmm(g.row_ptr, g.col_idx, g.vals, X, rows=rows)
                 b = 4 * (rows.size + 1) + 8 * enn + enn * F * 4 + rows.size * F * 4
             elif kind == "sddmm":
                 oracle.sddmm(g.row_ptr, g.col_idx, X, X, 1.0, rows=rows)
@@ -453,12 +465,14 @@ def cpu_baseline(graphs, budget_s=15.0, steps=1):
             tot_b += b
         return tot_b, tot_t
 
-    b, t = one_pass(4096)
-    stride = max(1, int(4096 * t / budget_s)) if t > 0 else 4096
-    b, t = one_pass(stride)
+    f0 = 1.0 / 2048
+    one_pass(f0)  # warm: features, transpose, thread pool
+    b, t = one_pass(f0)
+    frac = min(1.0, f0 * budget_s / t) if t > 0 else f0
+    b, t = one_pass(frac)
     return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"every {stride}-th row of each graph for every operation of the step "
-                      f"({b / 1e9:.2f} GB algorithmic, {t:.1f} s)"}
+            "sample": f"a seeded uniform {100 * frac:.2f}% of the rows of each graph for every operation of "
+                      f"the step ({b / 1e9:.2f} GB algorithmic, {t:.1f} s)"}
 
 
 def run_reference(args):

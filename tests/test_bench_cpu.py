@@ -1,0 +1,37 @@
+"""bench.py pieces that run without a GPU: the reference (oracle) arm's JSON
+line on a small graph, and the algorithmic byte formulas."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--scale", "11",
+                          "--steps", "1", "--warmup", "0", "--cpu-seconds", "0.5"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_algorithmic_bytes():
+    # SpMM: row_ptr + col_idx + vals + gathered rows + output rows
+    assert bench.spmm_bytes(10, 100, 4, 4) == 44 + 800 + 1600 + 160
+    # SDDMM: row_ptr + col_idx + Q rows + gathered K rows + scores
+    assert bench.sddmm_bytes(10, 100, 4, 4) == 44 + 400 + 160 + 1600 + 400
+    fused = bench.attn_bytes(10, 100, 2, 8, 2, True)
+    assert fused == 44 + 400 + 2 * 10 * 16 * 2 + 2 * 100 * 16 * 2
+    assert bench.attn_bytes(10, 100, 2, 8, 2, False) == fused + 5 * 4 * 100 * 2
+    ops = bench.op_list({"rmat": None, "uniform": None})
+    assert len(ops) == 2 * 2 * len(bench.FS) + 3
+    assert [k for k, *_ in ops][-3:] == ["spmm_t/rmat/F64", "attn_fused/rmat/H8D64", "attn_unfused/rmat/H8D64"]
