@@ -133,7 +133,7 @@ autosage_status choose_geom(DType dt, int H, int64_t D, std::initializer_list<Ma
   g.R = g.G;
   g.batched = false;
   if (H == 1) {
-    g.batched = g.G >= 4 && g.G <= 16;  // at 32 lanes the batch of 32 partial dots costs occupancy
+    g.batched = g.G >= 4;  // batches of 4 (G = 4) or 8 edges
   } else if (need_head_reduce) {
     if (!is_pow2(g.cph))
       return fail(AUTOSAGE_ERR_UNSUPPORTED, "multi-head reduction needs D/VW a power of two");

@@ -101,76 +101,80 @@ __global__ void __launch_bounds__(kBlock) sddmm_kernel(
   }
 }
 
-// Batched single-head SDDMM: G (compile time) feature lanes per edge lane.
-template <typename T, int VW, int NV, int G>
+// Batched single-head SDDMM: each edge lane's G feature lanes take B edges
+// at a time (B divides G). Every lane computes its partial dot for all B
+// edges; a transpose-reduction inside each aligned B-lane segment (B - 1
+// shuffles) leaves edge j's segment sum on lane j of the segment, and log2(G/B)
+// plain xor rounds add the segments. Lanes 0..B-1 then hold the B scores.
+template <typename T, int VW, int NV, int B>
 __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha, int es,
-    int nfrag, int E, float *__restrict__ S, ChunkList cl, int ipb) {
+    int nfrag, int G, int E, float *__restrict__ S, ChunkList cl, int ipb) {
   const Lanes L(G, E);
+  const int g = L.g;
+  const int base_lane = L.slot * L.GE + L.e * G;  // lane 0 of this edge lane's segment
+  constexpr int U = B < 4 ? B : 4;
   __shared__ int s_items;
   const ItemQueue queue(n_rows, cl, ipb, &s_items);
   int64_t idx;
   while (queue.next(L, idx)) {
-  const Item it = item_at(idx, n_rows, row_ptr, cl);
-  const int g = L.g;
-  float q[NV][VW];
+    const Item it = item_at(idx, n_rows, row_ptr, cl);
+    Frag<T, VW> q[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    Frag<T, VW> f;
-    const bool ok = it.active && it.e > it.b && g + k * G < nfrag;
-    if (ok) f.load(Q + it.row * ldq + (int64_t)(g + k * G) * VW);
-#pragma unroll
-    for (int v = 0; v < VW; ++v) q[k][v] = ok ? alpha * f.get(v) : 0.f;
-  }
-  // edges of this edge lane: p = it.b + e + E * t; batches of G consecutive t
-  const int first = it.b + L.e;
-  const int n_mine = it.e > first ? (it.e - first + E - 1) / E : 0;
-  const int base_lane = L.slot * L.GE + L.e * G;  // lane 0 of this edge lane's segment
-  constexpr int U = G < 4 ? G : 4;
-  for (int t0 = 0; t0 < n_mine; t0 += G) {
-    const int nb = min(G, n_mine - t0);
-    // one load brings the batch's column indices, lane j holding edge j's
-    const int pj = first + (t0 + g) * E;
-    const int my_col = g < nb ? ld_stream_i32(col_idx + pj) : 0;
-    float part[G];
-#pragma unroll
-    for (int j0 = 0; j0 < G; j0 += U) {
-      Frag<T, VW> f[U][NV];
-      int cj[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) cj[u] = __shfl_sync(L.sub_mask, my_col, base_lane + j0 + u);
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (j0 + u < nb && g + k * G < nfrag)
-            f[u][k].load(K + (int64_t)cj[u] * ldk + (int64_t)(g + k * G) * VW);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float d = 0.f;
-#pragma unroll
-        for (int k = 0; k < NV; ++k)
-          if (j0 + u < nb && g + k * G < nfrag)
-#pragma unroll
-            for (int v = 0; v < VW; ++v) d = fmaf(q[k][v], f[u][k].get(v), d);
-        part[j0 + u] = d;
-      }
+    for (int k = 0; k < NV; ++k) {
+      if (it.active && it.e > it.b && g + k * G < nfrag)
+        q[k].load(Q + it.row * ldq + (int64_t)(g + k * G) * VW);
+      else
+        q[k].zero();
     }
-    // transpose-reduce: after the stage on bit s, a lane keeps the half of the
-    // edges whose index has its own bit s, summed with its partner's half
+    // edges of this edge lane: p = it.b + e + E * t; batches of B consecutive t
+    const int first = it.b + L.e;
+    const int n_mine = it.e > first ? (it.e - first + E - 1) / E : 0;
+    for (int t0 = 0; t0 < n_mine; t0 += B) {
+      const int nb = min(B, n_mine - t0);
+      // one load brings the batch's column indices, lane j holding edge j's
+      const int pj = first + (t0 + g) * E;
+      const int my_col = g < nb ? ld_stream_i32(col_idx + pj) : 0;
+      float part[B];
 #pragma unroll
-    for (int sbit = G / 2; sbit >= 1; sbit >>= 1) {
-      const bool upper = (g & sbit) != 0;
+      for (int j0 = 0; j0 < B; j0 += U) {
+        Frag<T, VW> f[U][NV];
+        int cj[U];
 #pragma unroll
-      for (int i = 0; i < sbit; ++i) {
-        const float send = upper ? part[i] : part[i + sbit];
-        const float keep = upper ? part[i + sbit] : part[i];
-        part[i] = keep + __shfl_xor_sync(L.sub_mask, send, sbit);
+        for (int u = 0; u < U; ++u) cj[u] = __shfl_sync(L.sub_mask, my_col, base_lane + j0 + u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int k = 0; k < NV; ++k)
+            if (j0 + u < nb && g + k * G < nfrag)
+              f[u][k].load(K + (int64_t)cj[u] * ldk + (int64_t)(g + k * G) * VW);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          float d = 0.f;
+#pragma unroll
+          for (int k = 0; k < NV; ++k)
+            if (j0 + u < nb && g + k * G < nfrag)
+#pragma unroll
+              for (int v = 0; v < VW; ++v) d = fmaf(q[k].get(v), f[u][k].get(v), d);
+          part[j0 + u] = d;
+        }
       }
+      // after the stage on bit s, a lane keeps the half of the edges whose
+      // index has its own bit s, summed with its partner's half
+#pragma unroll
+      for (int sbit = B / 2; sbit >= 1; sbit >>= 1) {
+        const bool upper = (g & sbit) != 0;
+#pragma unroll
+        for (int i = 0; i < sbit; ++i) {
+          const float send = upper ? part[i] : part[i + sbit];
+          const float keep = upper ? part[i + sbit] : part[i];
+          part[i] = keep + __shfl_xor_sync(L.sub_mask, send, sbit);
+        }
+      }
+      for (int off = B; off < G; off <<= 1) part[0] += __shfl_xor_sync(L.sub_mask, part[0], off);
+      if (g < nb) S[(int64_t)pj * es] = alpha * part[0];
     }
-    if (g < nb) S[(int64_t)pj * es] = part[0];
-  }
   }
 }
 
@@ -178,17 +182,15 @@ template <typename T, int VW, int NV>
 cudaError_t launch_batched(const Geom &g, int64_t grid, int ipb, int64_t n_rows, const int32_t *row_ptr,
                            const int32_t *col_idx, const T *Q, int64_t ldq, const T *K, int64_t ldk,
                            float alpha, float *S, const ChunkList &cl, cudaStream_t s) {
-#define AUTOSAGE_SDDMM_B(GG)                                                                              \
-  sddmm_batched_kernel<T, VW, NV, GG><<<(unsigned)grid, kBlock, 0, s>>>(                           \
-      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.E, S, cl, ipb)
-  switch (g.G) {
-    case 2: AUTOSAGE_SDDMM_B(2); break;
-    case 4: AUTOSAGE_SDDMM_B(4); break;
-    case 8: AUTOSAGE_SDDMM_B(8); break;
-    case 16: AUTOSAGE_SDDMM_B(16); break;
-    case 32: AUTOSAGE_SDDMM_B(32); break;
-    default: return cudaErrorInvalidValue;
-  }
+#define AUTOSAGE_SDDMM_B(BB)                                                                              \
+  sddmm_batched_kernel<T, VW, NV, BB><<<(unsigned)grid, kBlock, 0, s>>>(                                \
+      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.G, g.E, S, cl, ipb)
+  if (g.G >= 8)
+    AUTOSAGE_SDDMM_B(8);
+  else if (g.G == 4)
+    AUTOSAGE_SDDMM_B(4);
+  else
+    return cudaErrorInvalidValue;
 #undef AUTOSAGE_SDDMM_B
   return cudaGetLastError();
 }
