@@ -61,6 +61,9 @@ def _bind(path: str):
     lib.oracle_transpose.argtypes = [_i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]
     lib.oracle_spmm_t_scatter.argtypes = [_i64, _i64, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _ptr]
     lib.oracle_row_stats.argtypes = [_i64, _ptr, _i64, _ptr, _ptr]
+    lib.oracle_csr_attention_backward.argtypes = [_i64, _i64, _ptr, _ptr, _i64, _i64, _ptr, _ptr, _ptr, _ptr,
+                                                  ctypes.c_double, _ptr, _ptr, _ptr]
+    lib.oracle_csr_attention_backward.restype = None
     lib.oracle_fingerprint.argtypes = [_i64, _ptr, _ptr]
     lib.oracle_fingerprint.restype = ctypes.c_uint64
     for name in ("oracle_spmm", "oracle_sddmm", "oracle_row_softmax", "oracle_csr_attention",
@@ -201,6 +204,23 @@ def csr_attention(row_ptr, col_idx, Q, K, V, heads: int, scale: float, rows=None
     lib.oracle_csr_attention(n_rows, _p(row_ptr), _p(col_idx), heads, F // heads, _p(Q), ldq,
                              _p(K), ldk, _p(V), ldv, float(scale), _p(r), n_out, _p(O))
     return O
+
+
+def csr_attention_backward(row_ptr, col_idx, Q, K, V, dO, heads: int, scale: float):
+    """Gradients (dQ, dK, dV) of CSR attention for an upstream gradient dO, in
+    double: the chain rule through the weighted sum and the row softmax."""
+    lib = _load()
+    row_ptr, col_idx = _i32(row_ptr), _i32(col_idx)
+    Q, K, V, dO = (np.ascontiguousarray(a, dtype=np.float32) for a in (Q, K, V, dO))
+    n_rows, n_cols, F = Q.shape[0], K.shape[0], Q.shape[1]
+    if F % heads or K.shape[1] != F or V.shape != K.shape or dO.shape != Q.shape:
+        raise ValueError("bad shapes")
+    dQ = np.zeros((n_rows, F))
+    dK = np.zeros((n_cols, F))
+    dV = np.zeros((n_cols, F))
+    lib.oracle_csr_attention_backward(n_rows, n_cols, _p(row_ptr), _p(col_idx), heads, F // heads, _p(Q), _p(K),
+                                      _p(V), _p(dO), float(scale), _p(dQ), _p(dK), _p(dV))
+    return dQ, dK, dV
 
 
 def edge_softmax_aggregate(row_ptr, col_idx, scores, V, heads: int = 1, rows=None):

@@ -237,3 +237,60 @@ uint64_t oracle_fingerprint(int64_t n_rows, const int32_t *row_ptr, const int32_
     h += splitmix64_mix(tag_cols ^ ((uint64_t)p << 32) ^ (uint32_t)col_idx[p]);
   return h;
 }
+
+/* Backward of CSR attention for a loss L with dL/dO = dO, per head h:
+ *   w_p = softmax over row i of s_p = scale * <Q[i], K[j]>     (j = col_idx[p])
+ *   dW_p = <dO[i], V[j]>,  D_i = sum_p w_p dW_p,  dS_p = w_p (dW_p - D_i)
+ *   dQ[i] = scale * sum_p dS_p K[j],   dK[j] += scale * dS_p Q[i],   dV[j] += w_p dO[i]
+ * (the chain rule through o_i = sum_p w_p v_j and the softmax). All in double.
+ * Q, dO, dQ have n_rows rows; K, V, dK, dV have n_cols rows; width H*D. */
+void oracle_csr_attention_backward(int64_t n_rows, int64_t n_cols, const int32_t *row_ptr,
+                                   const int32_t *col_idx, int64_t H, int64_t D, const float *Q,
+                                   const float *K, const float *V, const float *dO, double scale,
+                                   double *dQ, double *dK, double *dV) {
+  const int64_t F = H * D;
+  memset(dQ, 0, sizeof(double) * (size_t)(n_rows * F));
+  memset(dK, 0, sizeof(double) * (size_t)(n_cols * F));
+  memset(dV, 0, sizeof(double) * (size_t)(n_cols * F));
+  for (int64_t i = 0; i < n_rows; ++i) {
+    const int64_t b = row_ptr[i], e = row_ptr[i + 1];
+    if (e == b) continue;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(e - b));
+    double *dw = (double *)malloc(sizeof(double) * (size_t)(e - b));
+    for (int64_t h = 0; h < H; ++h) {
+      const float *q = Q + i * F + h * D;
+      const float *go = dO + i * F + h * D;
+      double m = -INFINITY;
+      for (int64_t p = b; p < e; ++p) {
+        const float *k = K + (int64_t)col_idx[p] * F + h * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d) acc += (double)q[d] * (double)k[d];
+        w[p - b] = scale * acc;
+        if (w[p - b] > m) m = w[p - b];
+      }
+      double sum = 0.0;
+      for (int64_t p = b; p < e; ++p) sum += exp(w[p - b] - m);
+      double Di = 0.0;
+      for (int64_t p = b; p < e; ++p) {
+        w[p - b] = exp(w[p - b] - m) / sum;
+        const float *v = V + (int64_t)col_idx[p] * F + h * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d) acc += (double)go[d] * (double)v[d];
+        dw[p - b] = acc;
+        Di += w[p - b] * acc;
+      }
+      for (int64_t p = b; p < e; ++p) {
+        const int64_t j = col_idx[p];
+        const double ds = w[p - b] * (dw[p - b] - Di);
+        const float *k = K + j * F + h * D;
+        for (int64_t d = 0; d < D; ++d) {
+          dQ[i * F + h * D + d] += scale * ds * (double)k[d];
+          dK[j * F + h * D + d] += scale * ds * (double)q[d];
+          dV[j * F + h * D + d] += w[p - b] * (double)go[d];
+        }
+      }
+    }
+    free(w);
+    free(dw);
+  }
+}

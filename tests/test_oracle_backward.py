@@ -1,0 +1,82 @@
+"""Pins for the oracle's CSR-attention backward (no GPU).
+
+The backward is checked against two things other than itself: central finite
+differences of the oracle's own forward (the definition of a derivative), and
+torch autograd through a dense masked attention in float64 on the CPU."""
+import numpy as np
+import pytest
+
+import oracle
+
+
+def small_graph(seed=0, n=9, m=7, p=0.5):
+    rng = np.random.default_rng(seed)
+    rows, cols = [], []
+    for i in range(n):
+        if i == 3:
+            continue  # one empty row
+        c = np.flatnonzero(rng.random(m) < p)
+        if c.size == 0:
+            c = np.array([i % m])
+        rows += [i] * c.size
+        cols += list(c)
+    row_ptr = np.zeros(n + 1, np.int32)
+    np.cumsum(np.bincount(np.array(rows), minlength=n), out=row_ptr[1:])
+    return row_ptr, np.array(cols, np.int32)
+
+
+def loss(row_ptr, col_idx, Q, K, V, dO, H, scale):
+    return float(np.sum(oracle.csr_attention(row_ptr, col_idx, Q, K, V, H, scale) * dO))
+
+
+@pytest.mark.parametrize("H,D", [(1, 3), (2, 2)])
+def test_backward_matches_finite_differences(H, D):
+    rp, ci = small_graph()
+    n, m, F = rp.size - 1, 7, H * D
+    rng = np.random.default_rng(1)
+    # values exactly representable in float32 with room for +-eps steps in double
+    Q, K, V, dO = (rng.standard_normal((r, F)).astype(np.float32) for r in (n, m, m, n))
+    scale = 0.7
+    dQ, dK, dV = oracle.csr_attention_backward(rp, ci, Q, K, V, dO, H, scale)
+    eps = 1e-3
+    for name, X, G in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        for idx in [(0, 0), (2, F - 1), (X.shape[0] - 1, 1 % F)]:
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += np.float32(eps)
+            Xm[idx] -= np.float32(eps)
+            step = float(Xp[idx]) - float(Xm[idx])
+            args = {"Q": Q, "K": K, "V": V}
+            args[name] = Xp
+            lp = loss(rp, ci, args["Q"], args["K"], args["V"], dO, H, scale)
+            args[name] = Xm
+            lm = loss(rp, ci, args["Q"], args["K"], args["V"], dO, H, scale)
+            fd = (lp - lm) / step
+            assert abs(fd - G[idx]) <= 2e-5 * (1 + abs(G[idx])), (name, idx, fd, G[idx])
+
+
+def test_backward_matches_torch_autograd_dense():
+    torch = pytest.importorskip("torch")
+    rp, ci = small_graph(seed=4, n=11, m=11, p=0.4)
+    n = rp.size - 1
+    H, D = 2, 3
+    rng = np.random.default_rng(2)
+    Q, K, V, dO = (rng.standard_normal((n, H * D)).astype(np.float32) for _ in range(4))
+    scale = 0.5
+    dQ, dK, dV = oracle.csr_attention_backward(rp, ci, Q, K, V, dO, H, scale)
+    mask = np.zeros((n, n), bool)
+    mask[np.repeat(np.arange(n), np.diff(rp)), ci] = True
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (Q, K, V))
+    out = []
+    for h in range(H):
+        sl = slice(h * D, (h + 1) * D)
+        s = scale * tq[:, sl] @ tk[:, sl].T
+        s = s.masked_fill(~torch.from_numpy(mask), float("-inf"))
+        has = torch.from_numpy(mask.any(axis=1))
+        w = torch.where(has[:, None], torch.softmax(s, dim=1), torch.zeros_like(s))
+        w = torch.nan_to_num(w)
+        out.append(w @ tv[:, sl])
+    o = torch.cat(out, dim=1)
+    (o * torch.from_numpy(dO.astype(np.float64))).sum().backward()
+    np.testing.assert_allclose(dQ, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dK, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dV, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
