@@ -109,6 +109,20 @@ def attn_bytes(n, nnz, H, D, s, fused):
     return b
 
 
+def attn_backward_bytes(n, m, nnz, H, D, s):
+    """Algorithmic bytes of one CSR-attention backward: the sum over its steps
+    (two SDDMMs, softmax, softmax backward, SpMM for dQ, the reorder of two edge
+    arrays, and the two SpMMs over A^T for dK and dV)."""
+    W = H * D
+    sddmm = 4 * (n + 1) + 4 * nnz + n * W * s + nnz * W * s + 4 * nnz * H
+    softmax = 3 * 4 * nnz * H
+    softmax_bwd = 4 * 4 * nnz * H
+    spmm_q = 4 * (n + 1) + 4 * nnz + 4 * nnz * H + nnz * W * s + n * W * s
+    permute = 4 * nnz + 4 * 4 * nnz * H
+    spmm_t = 4 * (m + 1) + 4 * nnz + 4 * nnz * H + nnz * W * s + m * W * s
+    return 2 * sddmm + softmax + softmax_bwd + spmm_q + permute + 2 * spmm_t
+
+
 def op_list(graphs, only=None):
     """(key, kind, graph, F) in execution order; graphs alternate so the other
     graph's data sits between two uses of one CSR. `only` keeps keys containing it."""
@@ -318,8 +332,40 @@ def run_ours(args):
         tot_nnzF += g.nnz * width
     step_ms, value = aggregate_ranks(tot_ms, tot_bytes, world, dev)
 
+    # rows beyond the step (SURVEY "next"): CSR-attention backward on the same graph
+    next_rows = {}
+    if not args.no_next and (not args.only or "backward" in args.only):
+        g = graphs["rmat"]
+        A = mats["rmat"]
+        W = HEADS * HEAD_DIM
+        bq, bk, bv, bo = (torch.randn(n, W, device=dev).to(torch.bfloat16)
+                          for n in (g.n_rows, g.n_cols, g.n_cols, g.n_rows))
+        bplan = sga.autosage_plan(A, sga.OP_ATTN_BACKWARD, HEAD_DIM, heads=HEADS, dtype=torch.bfloat16)
+        outs_b = [torch.empty_like(bq), torch.empty_like(bk), torch.empty_like(bv)]
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            sga.autosage_csr_attention_backward(A, bq, bk, bv, bo, HEADS, 0.125, *outs_b, plan=bplan)
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            sga.autosage_csr_attention_backward(A, bq, bk, bv, bo, HEADS, 0.125, *outs_b, plan=bplan)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+        b = attn_backward_bytes(g.n_rows, g.n_cols, g.nnz, HEADS, HEAD_DIM, 2)
+        peak_gbs, _ = measured_peak()
+        next_rows["attn_backward/rmat/H8D64"] = {
+            "ms": round(ms, 4), "GBps": round(b / ms / 1e6, 1), "frac_of_hbm_peak": round(b / ms / 1e6 / peak_gbs, 4),
+            "bytes": int(b), "dtype": "bf16 in/out, f32 accumulate", "plan": bplan.describe()}
+        del bq, bk, bv, bo, outs_b, bplan
+
     # dominant operation: the largest share of the step
-    dom_key = max(per_op, key=lambda k: per_op[k]["ms"])
+    # (one main kernel per launch: the unfused pipeline is three kernels, so it is not a candidate)
+    dom_key = max((k for k in per_op if not k.startswith("attn_unfused")), key=lambda k: per_op[k]["ms"])
     dom = per_op[dom_key]
     peak, peak_src = measured_peak()
     achieved = dom["GBps"]
@@ -396,6 +442,7 @@ def run_ours(args):
         "gpu_launches": n_launch,
         "plan_seconds": round(plan_s, 2),
         "per_op": per_op,
+        "next": next_rows,
         "source_hash": source_hash(),
     }
     if e2e is not None:
@@ -506,6 +553,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the rows measured beyond the step")
     ap.add_argument("--only", default=None, help="run only operations whose key contains this text")
     ap.add_argument("--scale", type=int, default=20, help="R-MAT scale (20 is the benchmark workload)")
     ap.add_argument("--cache", default=None, help="plan cache file: loaded if present, saved after planning")

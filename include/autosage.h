@@ -58,7 +58,8 @@ typedef enum {
   AUTOSAGE_OP_SDDMM = 2,         /* S = alpha * (Q K^T) sampled on A's pattern */
   AUTOSAGE_OP_ATTN = 3,          /* fused CSR attention */
   AUTOSAGE_OP_ATTN_UNFUSED = 4,  /* SDDMM -> row softmax -> SpMM with scores in HBM */
-  AUTOSAGE_OP_SOFTMAX = 5        /* per-row softmax of edge scores */
+  AUTOSAGE_OP_SOFTMAX = 5,       /* per-row softmax of edge scores */
+  AUTOSAGE_OP_ATTN_BACKWARD = 6  /* gradients of CSR attention (plan holds A^T) */
 } autosage_op;
 
 /* Schedule families the planner chooses among (all are this library's own kernels). */
@@ -132,6 +133,23 @@ autosage_status autosage_csr_attention(const autosage_csr *A, const void *Q, con
                                        const void *V, int heads, int64_t D, autosage_dtype dt,
                                        float scale, void *out, int fused, autosage_plan_t plan,
                                        void *stream);
+
+/* Backward of CSR attention (the chain rule through the composition SDDMM -> row-softmax
+ * -> SpMM of the Abstract): for the upstream gradient dO [n_rows, heads, D], per head,
+ *   w = softmax over row i of scale * <Q[i], K[j]>,  dW_p = <dO[i], V[j]>,
+ *   dS_p = w_p (dW_p - sum_q w_q dW_q),
+ *   dQ[i] = scale * sum_p dS_p K[j],  dK[j] = scale * sum_{p: col(p)=j} dS_p Q[i],
+ *   dV[j] = sum_{p: col(p)=j} w_p dO[i].
+ * The weights are recomputed from Q and K (SDDMM + softmax), dW is an SDDMM, dQ an SpMM
+ * over A, dK and dV SpMMs over A^T with the edge arrays reordered into A^T's edge order.
+ * Q, dO, dQ have n_rows rows; K, V, dK, dV have n_cols rows; all [., heads, D] of type dt,
+ * contiguous. plan: built for AUTOSAGE_OP_ATTN_BACKWARD with F = D (it holds A^T, the
+ * permutation and the edge buffers); NULL builds a temporary plan inside the call, which
+ * allocates device memory and SYNCHRONISES `stream`. */
+autosage_status autosage_csr_attention_backward(const autosage_csr *A, const void *Q, const void *K,
+                                                const void *V, const void *dO, int heads, int64_t D,
+                                                autosage_dtype dt, float scale, void *dQ, void *dK,
+                                                void *dV, autosage_plan_t plan, void *stream);
 
 /* The benchmark page's op (fused softmax + aggregation with given scores): per head,
  * w = softmax over row i of scores[p, h]; out[i,h,:] = sum_p w_p V[col_idx[p],h,:].

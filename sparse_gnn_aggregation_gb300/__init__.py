@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libautosage.so")
 OK, ERR_INVALID_ARG, ERR_INVALID_CSR, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
 ERR_CACHE_IO, ERR_CACHE_FORMAT, ERR_PROBE, ERR_PLAN_MISMATCH = 5, 6, 7, 8
 F32, BF16 = 0, 1
-OP_SPMM, OP_SPMM_T, OP_SDDMM, OP_ATTN, OP_ATTN_UNFUSED, OP_SOFTMAX = 0, 1, 2, 3, 4, 5
+OP_SPMM, OP_SPMM_T, OP_SDDMM, OP_ATTN, OP_ATTN_UNFUSED, OP_SOFTMAX, OP_ATTN_BACKWARD = 0, 1, 2, 3, 4, 5, 6
 SCHED_AUTO, SCHED_ROWGROUP, SCHED_SPLIT, SCHED_MERGEPATH = -1, 0, 1, 2
 PLAN_PROBE, PLAN_NO_CACHE, PLAN_VERIFY = 1, 2, 4
 
@@ -38,7 +38,7 @@ EXPORTS = [
     "autosage_cache_load", "autosage_cache_save", "autosage_cache_clear", "autosage_cache_size",
     "autosage_row_stats", "autosage_fingerprint", "autosage_validate_csr", "autosage_csr_transpose",
     "autosage_status_string", "autosage_last_error", "autosage_version",
-    "autosage_csr_attention_unfused_noalloc",
+    "autosage_csr_attention_unfused_noalloc", "autosage_csr_attention_backward",
 ]
 
 
@@ -71,6 +71,7 @@ def _load():
         "autosage_row_softmax": [CSR, P, I, P, P],
         "autosage_csr_attention": [CSR, P, P, P, I, I64, I, F, P, I, P, P],
         "autosage_csr_attention_unfused_noalloc": [CSR, P, P, P, I, I64, I, F, P, P],
+        "autosage_csr_attention_backward": [CSR, P, P, P, P, I, I64, I, F, P, P, P, P, P],
         "autosage_edge_softmax_aggregate": [CSR, P, P, I, I64, I, P, P, P],
         "autosage_plan": [CSR, I, I64, I, I, U, ctypes.POINTER(P), P],
         "autosage_plan_with_schedule": [CSR, I, I64, I, I, ctypes.POINTER(_Schedule), ctypes.POINTER(P), P],
@@ -298,6 +299,27 @@ def autosage_csr_attention(A: CsrMatrix, Q, K, V, heads: int, scale: float, fuse
     _check(_lib.autosage_csr_attention(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), D, _dt(Q), float(scale),
                                        _ptr(out), int(bool(fused)), _plan_handle(plan), _stream(stream)))
     return out
+
+
+def autosage_csr_attention_backward(A: CsrMatrix, Q, K, V, dO, heads: int, scale: float, dQ=None, dK=None,
+                                    dV=None, plan: Plan | None = None, stream=None):
+    """Gradients (dQ, dK, dV) of CSR attention for the upstream gradient dO.
+
+    All tensors are [n, heads * D] contiguous of one dtype. ``plan`` should be
+    built for OP_ATTN_BACKWARD with F = D; without one the call builds a
+    temporary plan (allocating and synchronising)."""
+    torch = _torch()
+    W = int(Q.shape[-1]) if Q.dim() == 2 else int(Q.shape[-1] * Q.shape[-2])
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    for t in (Q, K, V, dO, dQ, dK, dV):
+        if not t.is_contiguous() or t.dtype != Q.dtype:
+            raise ValueError("backward tensors must be contiguous and share one dtype")
+    _check(_lib.autosage_csr_attention_backward(A.c, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), int(heads), W // heads,
+                                                _dt(Q), float(scale), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                                _plan_handle(plan), _stream(stream)))
+    return dQ, dK, dV
 
 
 NOALLOC_MAX_SCORES = 4 * 1024 * 1024

@@ -431,7 +431,7 @@ cudaError_t build_chunk_lists(int64_t n_rows, const int32_t *row_ptr, int split,
 
 cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *row_ptr,
                           const int32_t *col_idx, const float *vals, int32_t *row_ptr_t,
-                          int32_t *col_idx_t, float *vals_t, cudaStream_t s) {
+                          int32_t *col_idx_t, float *vals_t, int32_t *perm, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   // row_ptr_t = exclusive scan of the column counts
   int32_t *counts = nullptr;
@@ -472,6 +472,9 @@ cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int
       transpose_gather_kernel<<<(unsigned)((nnz + 255) / 256), 256, 0, s>>>(
           nnz, va, rows, vals, col_idx_t, vals ? vals_t : nullptr);
       err = cudaGetLastError();
+      // position k of A^T holds edge va[k] of A
+      if (err == cudaSuccess && perm)
+        err = cudaMemcpyAsync(perm, va, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDeviceToDevice, s);
     }
     for (int i = 0; i < 7; ++i)
       if (*bufs[i]) cudaFreeAsync(*bufs[i], s);

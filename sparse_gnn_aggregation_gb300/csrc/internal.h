@@ -90,9 +90,18 @@ cudaError_t build_chunk_lists(int64_t n_rows, const int32_t *row_ptr, int split,
                               int32_t *long_ptr, int32_t *chunk_row, int32_t *chunk_begin,
                               int64_t *n_long_out, int64_t *n_chunks_out, cudaStream_t s);
 // Stable transpose by LSD radix sort; temporaries from cudaMallocAsync on s.
+// perm (optional, [nnz]): position k of A^T holds edge perm[k] of A.
 cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *row_ptr,
                           const int32_t *col_idx, const float *vals, int32_t *row_ptr_t,
-                          int32_t *col_idx_t, float *vals_t, cudaStream_t s);
+                          int32_t *col_idx_t, float *vals_t, int32_t *perm, cudaStream_t s);
+// Softmax backward in place: dS <- scale * W * (dS - rowsum(W * dS)) per row and head.
+// part: [n_chunks * H] fp32 + [n_chunks] int32, row_d: [n_long * H] fp32 (cut rows only).
+cudaError_t launch_softmax_backward(int64_t n_rows, const int32_t *row_ptr, int H, const float *W, float *dS,
+                                    float scale, const ChunkList &cl, float *part, float *row_d,
+                                    cudaStream_t s);
+// out_a[k, :] = a[perm[k], :], out_b[k, :] = b[perm[k], :] (rows of H floats).
+cudaError_t launch_permute_edges(int64_t nnz, int H, const int32_t *perm, const float *a, const float *b,
+                                 float *out_a, float *out_b, cudaStream_t s);
 // Deterministic pseudo-random fill of probe buffers (values in [-1, 1)).
 cudaError_t fill_probe(void *p, int64_t n_elems, DType dt, uint64_t seed, cudaStream_t s);
 // Count elements with |a - b| > atol + rtol * |b| (fp32 or bf16 arrays) into *count (device).

@@ -253,13 +253,17 @@ struct autosage_plan_s {
   // merge-path workspace
   DevBuf mp_part, mp_carry_val, mp_carry_row;
   int64_t mp_warps = 0;
-  // unfused attention scores
+  // unfused attention scores (backward: the softmax weights)
   DevBuf scores;
+  // A^T position -> A edge (SPMM_T); backward edge buffers and the A^T SpMM plan
+  DevBuf t_perm, grad_dw, grad_wt, grad_dst;
+  autosage_plan_s *tplan = nullptr;
   ~autosage_plan_s() {
     for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
                       &chunk_begin, &partial, &ml, &row_ml, &mp_part, &mp_carry_val,
-                      &mp_carry_row, &scores})
+                      &mp_carry_row, &scores, &t_perm, &grad_dw, &grad_wt, &grad_dst})
       b->release();
+    delete tplan;
   }
 };
 
@@ -311,6 +315,7 @@ OpShape op_shape(autosage_op op, int64_t F, int H) {
     case AUTOSAGE_OP_ATTN: return {H, F, true, 8};
     case AUTOSAGE_OP_ATTN_UNFUSED: return {H, F, true, 16};
     case AUTOSAGE_OP_SOFTMAX: return {H, 1, false, 16};
+    case AUTOSAGE_OP_ATTN_BACKWARD: return {H, F, true, 16};
   }
   return {1, F, false, 16};
 }
@@ -358,11 +363,12 @@ autosage_status build_split(autosage_plan_s *P, int split, cudaStream_t s) {
   P->cl.split = split;
   // partial buffers for every consumer of the chunk list
   const int64_t C = got_chunks;
-  const int64_t width = P->F * (P->op == AUTOSAGE_OP_ATTN || P->op == AUTOSAGE_OP_ATTN_UNFUSED ? P->H : 1);
+  const bool heads_op = P->op == AUTOSAGE_OP_ATTN || P->op == AUTOSAGE_OP_ATTN_UNFUSED ||
+                        P->op == AUTOSAGE_OP_ATTN_BACKWARD;
+  const int64_t width = P->F * (heads_op ? P->H : 1);
   if (P->op != AUTOSAGE_OP_SDDMM && P->op != AUTOSAGE_OP_SOFTMAX)
     CUDA_TRY(P->partial.alloc(sizeof(float) * (size_t)std::max<int64_t>(C * width, 1)));
-  const int Hs = (P->op == AUTOSAGE_OP_SOFTMAX || P->op == AUTOSAGE_OP_ATTN ||
-                  P->op == AUTOSAGE_OP_ATTN_UNFUSED) ? P->H : 1;
+  const int Hs = (P->op == AUTOSAGE_OP_SOFTMAX || heads_op) ? P->H : 1;
   CUDA_TRY(P->ml.alloc(sizeof(float) * (size_t)std::max<int64_t>(C * Hs * 2 + C, 1)));
   CUDA_TRY(P->row_ml.alloc(sizeof(float) * (size_t)std::max<int64_t>(n_long * Hs * 2, 1)));
   return AUTOSAGE_OK;
@@ -387,7 +393,7 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
   P->cl = ChunkList{};
   P->mp_warps = 0;
   autosage_status st = AUTOSAGE_OK;
-  if (P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) {
+  if (P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T || P->op == AUTOSAGE_OP_ATTN_BACKWARD) {
     if (P->maxdeg < 0) {
       RowStats rs;
       st = gpu_row_stats(P->k_rows, P->k_row_ptr, 1024, rs, s);
@@ -409,8 +415,14 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
     st = build_mergepath(P, P->sched.split, P->F, s);
   }
   if (st != AUTOSAGE_OK) return st;
-  if (P->op == AUTOSAGE_OP_ATTN_UNFUSED && !P->scores.p)
+  if ((P->op == AUTOSAGE_OP_ATTN_UNFUSED || P->op == AUTOSAGE_OP_ATTN_BACKWARD) && !P->scores.p)
     CUDA_TRY(P->scores.alloc(sizeof(float) * (size_t)std::max<int64_t>(P->nnz * P->H, 1)));
+  if (P->op == AUTOSAGE_OP_ATTN_BACKWARD && !P->grad_dw.p) {
+    const size_t eb = sizeof(float) * (size_t)std::max<int64_t>(P->nnz * P->H, 1);
+    CUDA_TRY(P->grad_dw.alloc(eb));
+    CUDA_TRY(P->grad_wt.alloc(eb));
+    CUDA_TRY(P->grad_dst.alloc(eb));
+  }
   CUDA_TRY(cudaStreamSynchronize(s));
   return AUTOSAGE_OK;
 }
@@ -427,6 +439,8 @@ struct OpArgs {
   float alpha = 1.f;
   float *S = nullptr;       // SDDMM output / softmax in-out
   const float *given = nullptr;  // given scores (edge-softmax aggregation)
+  const void *dO = nullptr;      // backward: upstream gradient and outputs
+  void *dQ = nullptr, *dK = nullptr, *dV = nullptr;
 };
 
 // Run `op` with plan P's schedule (plan-free runs use a transient P with
@@ -537,6 +551,54 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
                       P->partial.as<float>(), s);
       break;
     }
+    case AUTOSAGE_OP_ATTN_BACKWARD: {
+      const autosage_plan_s *T = P->tplan;
+      if (!T) return fail(AUTOSAGE_ERR_INVALID_ARG, "backward plan lacks its A^T part");
+      const int64_t ld = P->H * P->F;
+      float *W = P->scores.as<float>(), *dS = P->grad_dw.as<float>();
+      // weights: SDDMM(Q, K) * scale, then the row softmax
+      st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}}, P->sched.G, P->sched.E, true, 16, g);
+      if (st != AUTOSAGE_OK) return st;
+      e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, ld, a.K, ld, a.alpha, W, cl, s);
+      if (e == cudaSuccess)
+        e = launch_row_softmax(P->k_rows, P->k_row_ptr, P->H, W, cl, P->ml.as<float>(), P->row_ml.as<float>(), s);
+      // dW = SDDMM(dO, V); dS = scale * W * (dW - rowsum(W * dW)) in place
+      if (e == cudaSuccess) {
+        st = choose_geom(P->dt, P->H, P->F, {{a.dO, ld}, {a.X, ld}}, P->sched.G, P->sched.E, true, 16, g);
+        if (st != AUTOSAGE_OK) return st;
+        e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.dO, ld, a.X, ld, 1.f, dS, cl, s);
+      }
+      if (e == cudaSuccess)
+        e = launch_softmax_backward(P->k_rows, P->k_row_ptr, P->H, W, dS, a.alpha, cl, P->ml.as<float>(),
+                                    P->row_ml.as<float>(), s);
+      // dQ = SpMM(A; dS, K)
+      if (e == cudaSuccess) {
+        st = choose_geom(P->dt, P->H, P->F, {{a.K, ld}, {a.dQ, ld}}, P->sched.G, P->sched.E, false, 16, g);
+        if (st != AUTOSAGE_OK) return st;
+        g.comp = P->comp;
+        e = launch_spmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, dS, a.K, ld, a.dQ, ld, cl,
+                        P->partial.as<float>(), s);
+      }
+      // W and dS in the edge order of A^T, then dV = SpMM(A^T; W, dO), dK = SpMM(A^T; dS, Q)
+      if (e == cudaSuccess)
+        e = launch_permute_edges(P->nnz, P->H, T->t_perm.as<int32_t>(), W, dS, P->grad_wt.as<float>(),
+                                 P->grad_dst.as<float>(), s);
+      if (e == cudaSuccess) {
+        st = choose_geom(P->dt, P->H, P->F, {{a.dO, ld}, {a.dV, ld}}, T->sched.G, T->sched.E, false, 16, g);
+        if (st != AUTOSAGE_OK) return st;
+        g.comp = T->comp;
+        e = launch_spmm(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_wt.as<float>(), a.dO, ld, a.dV, ld,
+                        T->cl, T->partial.as<float>(), s);
+      }
+      if (e == cudaSuccess) {
+        st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.dK, ld}}, T->sched.G, T->sched.E, false, 16, g);
+        if (st != AUTOSAGE_OK) return st;
+        g.comp = T->comp;
+        e = launch_spmm(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_dst.as<float>(), a.Q, ld, a.dK, ld,
+                        T->cl, T->partial.as<float>(), s);
+      }
+      break;
+    }
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return AUTOSAGE_OK;
@@ -614,12 +676,13 @@ autosage_status make_plan_shell(const autosage_csr *A, autosage_op op, int64_t F
   if (F < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "F must be >= 1");
   if (heads < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads must be >= 1");
   if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
-  if (op < AUTOSAGE_OP_SPMM || op > AUTOSAGE_OP_SOFTMAX) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad op");
+  if (op < AUTOSAGE_OP_SPMM || op > AUTOSAGE_OP_ATTN_BACKWARD) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad op");
   auto *P = new autosage_plan_s();
   P->op = op;
   P->dt = static_cast<DType>(dt);
   P->F = (op == AUTOSAGE_OP_SOFTMAX) ? 1 : F;
-  P->H = (op == AUTOSAGE_OP_ATTN || op == AUTOSAGE_OP_ATTN_UNFUSED || op == AUTOSAGE_OP_SOFTMAX) ? heads : 1;
+  P->H = (op == AUTOSAGE_OP_ATTN || op == AUTOSAGE_OP_ATTN_UNFUSED || op == AUTOSAGE_OP_SOFTMAX ||
+          op == AUTOSAGE_OP_ATTN_BACKWARD) ? heads : 1;
   P->n_rows = A->n_rows;
   P->n_cols = A->n_cols;
   P->nnz = A->nnz;
@@ -631,9 +694,11 @@ autosage_status make_plan_shell(const autosage_csr *A, autosage_op op, int64_t F
     cudaError_t e = P->t_row_ptr.alloc(sizeof(int32_t) * (size_t)(A->n_cols + 1));
     if (e == cudaSuccess) e = P->t_col_idx.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(A->nnz, 1));
     if (e == cudaSuccess && A->vals) e = P->t_vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(A->nnz, 1));
+    if (e == cudaSuccess) e = P->t_perm.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(A->nnz, 1));
     if (e == cudaSuccess)
       e = csr_transpose(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx, A->vals,
-                        P->t_row_ptr.as<int32_t>(), P->t_col_idx.as<int32_t>(), P->t_vals.as<float>(), s);
+                        P->t_row_ptr.as<int32_t>(), P->t_col_idx.as<int32_t>(), P->t_vals.as<float>(),
+                        P->t_perm.as<int32_t>(), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
       delete P;
@@ -803,6 +868,32 @@ void log_line(const char *fmt, ...) {
   fclose(f);
 }
 
+// The backward plan: the forward-direction workspace (weights, dW/dS, chunk
+// lists of A) plus an SpMM plan over A^T (transposed CSR, edge permutation,
+// its own chunk lists). Rows longer than the chunk length are cut in both
+// directions; shorter rows run whole, so one chunk length serves every graph.
+autosage_status build_backward_plan(autosage_plan_s *P, const Sched &sc, cudaStream_t s) {
+  P->sched = sc;
+  if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) P->sched = Sched{AUTOSAGE_SCHED_SPLIT, sc.G, sc.E, sc.split};
+  autosage_status st = build_workspace(P, s);
+  if (st != AUTOSAGE_OK) return st;
+  autosage_csr A{P->n_rows, P->n_cols, P->nnz, P->k_row_ptr, P->k_col_idx, P->k_vals};
+  autosage_plan_s *T = nullptr;
+  st = make_plan_shell(&A, AUTOSAGE_OP_SPMM_T, P->F * P->H, 1, static_cast<autosage_dtype>(P->dt), &T, s);
+  if (st != AUTOSAGE_OK) return st;
+  T->sched = Sched{P->sched.kind, 0, 0, P->sched.split};
+  st = build_workspace(T, s);
+  if (st != AUTOSAGE_OK) {
+    delete T;
+    return st;
+  }
+  delete P->tplan;
+  P->tplan = T;
+  return AUTOSAGE_OK;
+}
+
+Sched default_backward_sched() { return Sched{AUTOSAGE_SCHED_SPLIT, 0, 0, 128}; }
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -848,6 +939,15 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
   if (P->sched.kind == AUTOSAGE_SCHED_SPLIT && P->sched.split == 0) P->sched.split = 1024;
   if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH && P->sched.split == 0) P->sched.split = 512;
   if (P->sched.kind == AUTOSAGE_SCHED_ROWGROUP) P->sched.split = 0;
+  if (op == AUTOSAGE_OP_ATTN_BACKWARD) {
+    st = build_backward_plan(P, P->sched, s);
+    if (st != AUTOSAGE_OK) {
+      delete P;
+      return st;
+    }
+    *out = P;
+    return AUTOSAGE_OK;
+  }
   st = build_workspace(P, s);
   if (st != AUTOSAGE_OK) {
     delete P;
@@ -865,6 +965,15 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
   autosage_plan_s *P = nullptr;
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
+  if (op == AUTOSAGE_OP_ATTN_BACKWARD) {  // fixed schedule: cut rows longer than 128 edges
+    st = build_backward_plan(P, default_backward_sched(), s);
+    if (st != AUTOSAGE_OK) {
+      delete P;
+      return st;
+    }
+    *out = P;
+    return AUTOSAGE_OK;
+  }
   const DeviceInfo dev = device_info();
   // structure statistics and fingerprint of the CSR the kernels walk
   RowStats rs;
@@ -1207,6 +1316,41 @@ autosage_status autosage_edge_softmax_aggregate(const autosage_csr *A, const flo
   return run_op(&P, AUTOSAGE_OP_ATTN, a, as_stream(stream));
 }
 
+autosage_status autosage_csr_attention_backward(const autosage_csr *A, const void *Q, const void *K,
+                                                const void *V, const void *dO, int heads, int64_t D,
+                                                autosage_dtype dt, float scale, void *dQ, void *dK,
+                                                void *dV, autosage_plan_t plan, void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (heads < 1 || D < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads and D must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  const int64_t W = (int64_t)heads * D;
+  if ((st = check_mat(Q, W, W, A->n_rows, "Q")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(dO, W, W, A->n_rows, "dO")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(dQ, W, W, A->n_rows, "dQ")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(K, W, W, A->n_cols, "K")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(V, W, W, A->n_cols, "V")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(dK, W, W, A->n_cols, "dK")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(dV, W, W, A->n_cols, "dV")) != AUTOSAGE_OK) return st;
+  if (A->n_rows == 0 && A->n_cols == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.Q = Q; a.K = K; a.X = V; a.dO = dO; a.dQ = dQ; a.dK = dK; a.dV = dV; a.alpha = scale;
+  cudaStream_t s = as_stream(stream);
+  if (plan) {
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_ATTN_BACKWARD, D, heads, dt)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_ATTN_BACKWARD, a, s);
+  }
+  autosage_plan_s *P = nullptr;
+  st = make_plan_shell(A, AUTOSAGE_OP_ATTN_BACKWARD, D, heads, dt, &P, s);
+  if (st != AUTOSAGE_OK) return st;
+  st = build_backward_plan(P, default_backward_sched(), s);
+  if (st == AUTOSAGE_OK) st = run_op(P, AUTOSAGE_OP_ATTN_BACKWARD, a, s);
+  cudaError_t e = cudaStreamSynchronize(s);
+  delete P;
+  if (st == AUTOSAGE_OK && e != cudaSuccess) return cuda_fail(e, "attention backward");
+  return st;
+}
+
 // ---------------------------------------------------------------- utilities
 
 autosage_status autosage_row_stats(const autosage_csr *A, int64_t long_threshold, int64_t *ints, double *reals,
@@ -1266,7 +1410,7 @@ autosage_status autosage_csr_transpose(const autosage_csr *A, int32_t *row_ptr_t
   if (st != AUTOSAGE_OK) return st;
   if (!row_ptr_t || (A->nnz > 0 && !col_idx_t)) return fail(AUTOSAGE_ERR_INVALID_ARG, "output is NULL");
   cudaError_t e = csr_transpose(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx,
-                                vals_t ? A->vals : nullptr, row_ptr_t, col_idx_t, vals_t,
+                                vals_t ? A->vals : nullptr, row_ptr_t, col_idx_t, vals_t, nullptr,
                                 as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "transpose");
   return AUTOSAGE_OK;
