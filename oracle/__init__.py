@@ -64,6 +64,8 @@ def _bind(path: str):
     lib.oracle_csr_attention_backward.argtypes = [_i64, _i64, _ptr, _ptr, _i64, _i64, _ptr, _ptr, _ptr, _ptr,
                                                   ctypes.c_double, _ptr, _ptr, _ptr]
     lib.oracle_csr_attention_backward.restype = None
+    lib.oracle_spmm_typed.argtypes = [_i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _ptr]
+    lib.oracle_spmm_typed.restype = None
     lib.oracle_fingerprint.argtypes = [_i64, _ptr, _ptr]
     lib.oracle_fingerprint.restype = ctypes.c_uint64
     for name in ("oracle_spmm", "oracle_sddmm", "oracle_row_softmax", "oracle_csr_attention",
@@ -221,6 +223,21 @@ def csr_attention_backward(row_ptr, col_idx, Q, K, V, dO, heads: int, scale: flo
     lib.oracle_csr_attention_backward(n_rows, n_cols, _p(row_ptr), _p(col_idx), heads, F // heads, _p(Q), _p(K),
                                       _p(V), _p(dO), float(scale), _p(dQ), _p(dK), _p(dV))
     return dQ, dK, dV
+
+
+def spmm_typed(row_ptr, col_idx, edge_type, vals, Z):
+    """Multi-relation SpMM: Y[i] = sum_p vals[p] Z[edge_type[p], col_idx[p]]; Z is [R, n_cols, F]."""
+    lib = _load()
+    row_ptr, col_idx, edge_type = _i32(row_ptr), _i32(col_idx), _i32(edge_type)
+    Z = np.ascontiguousarray(Z, dtype=np.float32)
+    R, n_cols, F = Z.shape
+    if edge_type.size and (edge_type.min() < 0 or edge_type.max() >= R):
+        raise ValueError("edge type out of range")
+    v = None if vals is None else _f32(vals)
+    Y = np.zeros((row_ptr.size - 1, F))
+    lib.oracle_spmm_typed(row_ptr.size - 1, n_cols, _p(row_ptr), _p(col_idx), _p(edge_type), _p(v),
+                          _p(Z.reshape(R * n_cols, F)), F, F, _p(Y))
+    return Y
 
 
 def edge_softmax_aggregate(row_ptr, col_idx, scores, V, heads: int = 1, rows=None):

@@ -294,3 +294,21 @@ void oracle_csr_attention_backward(int64_t n_rows, int64_t n_cols, const int32_t
     free(dw);
   }
 }
+
+/* Multi-relation (typed) SpMM, the aggregation of an RGCN-style layer:
+ * Y[i, :] = sum_p vals[p] * Z[edge_type[p], col_idx[p], :], with Z holding one
+ * [n_cols, F] block per relation (block r starts at row r * n_cols). */
+void oracle_spmm_typed(int64_t n_rows, int64_t n_cols, const int32_t *row_ptr, const int32_t *col_idx,
+                       const int32_t *edge_type, const float *vals, const float *Z, int64_t ldz,
+                       int64_t F, double *Y) {
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t i = 0; i < n_rows; ++i) {
+    double *y = Y + i * F;
+    for (int64_t f = 0; f < F; ++f) y[f] = 0.0;
+    for (int64_t p = row_ptr[i]; p < row_ptr[i + 1]; ++p) {
+      const double w = vals ? (double)vals[p] : 1.0;
+      const float *z = Z + ((int64_t)edge_type[p] * n_cols + col_idx[p]) * ldz;
+      for (int64_t f = 0; f < F; ++f) y[f] += w * (double)z[f];
+    }
+  }
+}
