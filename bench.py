@@ -53,14 +53,29 @@ def dist_env():
     return rank, world, local
 
 
-def source_hash() -> str:
+KERNEL_FILES = {
+    "spmm": ["spmm.cu", "common.cuh"],
+    "spmm_t": ["spmm.cu", "graph.cu", "common.cuh"],
+    "sddmm": ["sddmm.cu", "common.cuh"],
+    "attn_fused": ["attention.cu", "common.cuh"],
+    "attn_unfused": ["sddmm.cu", "softmax.cu", "spmm.cu", "common.cuh"],
+}
+
+
+def source_hash(files=None) -> str:
+    """Hash of kernel sources (all of csrc/, or the listed files)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_gnn_aggregation_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files or os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def kernel_hash(op_key: str) -> str:
+    """Hash of the sources that define the kernels of an operation key like 'attn_fused/rmat/H8D64'."""
+    return source_hash(KERNEL_FILES.get(op_key.split("/")[0]))
 
 
 def measured_peak():
@@ -77,7 +92,7 @@ def traffic_for(op_key: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = source_hash()
+    cur = kernel_hash(op_key)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -362,6 +377,35 @@ def run_ours(args):
             "ms": round(ms, 4), "GBps": round(b / ms / 1e6, 1), "frac_of_hbm_peak": round(b / ms / 1e6 / peak_gbs, 4),
             "bytes": int(b), "dtype": "bf16 in/out, f32 accumulate", "plan": bplan.describe()}
         del bq, bk, bv, bo, outs_b, bplan
+    if not args.no_next and (not args.only or "typed" in args.only):
+        # multi-relation SpMM (RGCN-style): 4 relations, F = 64, fp32
+        g = graphs["rmat"]
+        A = mats["rmat"]
+        R, F = 4, 64
+        et = torch.from_numpy(synth.rng_for(0, 9).integers(0, R, g.nnz).astype(np.int32)).to(dev)
+        Z = torch.randn(R, g.n_cols, F, device=dev)
+        Yt = torch.empty(g.n_rows, F, device=dev)
+        tplan = sga.autosage_plan_typed(A, et, R, F, flags=sga.PLAN_PROBE | sga.PLAN_VERIFY)
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            sga.autosage_spmm_typed(A, et, Z, Yt, plan=tplan)
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            sga.autosage_spmm_typed(A, et, Z, Yt, plan=tplan)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+        b = spmm_bytes(g.n_rows, g.nnz, F, 4)
+        peak_gbs, _ = measured_peak()
+        next_rows["spmm_typed/rmat/R4F64"] = {
+            "ms": round(ms, 4), "GBps": round(b / ms / 1e6, 1), "frac_of_hbm_peak": round(b / ms / 1e6 / peak_gbs, 4),
+            "bytes": int(b), "dtype": "f32", "plan": tplan.describe()}
+        del et, Z, Yt, tplan
 
     # dominant operation: the largest share of the step
     # (one main kernel per launch: the unfused pipeline is three kernels, so it is not a candidate)

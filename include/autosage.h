@@ -134,6 +134,21 @@ autosage_status autosage_csr_attention(const autosage_csr *A, const void *Q, con
                                        float scale, void *out, int fused, autosage_plan_t plan,
                                        void *stream);
 
+/* Multi-relation (typed) SpMM, the aggregation of an RGCN-style layer (SparseTIR's
+ * RGCN workload): Y[i,:] = sum_p vals[p] * Z[edge_type[p] * n_cols + col_idx[p], :].
+ * Z stacks one [n_cols, F] feature block per relation (typically X W_r computed by a
+ * dense GEMM), row stride ldz, type dt. edge_type is a device int32 [nnz] array with
+ * values in [0, num_types). The plan (autosage_plan_typed) checks the types on the GPU,
+ * stores the combined gather index and picks an SpMM schedule for it; plan == NULL
+ * builds a temporary plan inside the call (allocates and SYNCHRONISES `stream`).
+ * num_types * n_cols must fit int32. */
+autosage_status autosage_plan_typed(const autosage_csr *A, const int32_t *edge_type, int num_types,
+                                    int64_t F, autosage_dtype dt, unsigned flags,
+                                    autosage_plan_t *out, void *stream);
+autosage_status autosage_spmm_typed(const autosage_csr *A, const int32_t *edge_type, int num_types,
+                                    const void *Z, int64_t ldz, void *Y, int64_t ldy, int64_t F,
+                                    autosage_dtype dt, autosage_plan_t plan, void *stream);
+
 /* Backward of CSR attention (the chain rule through the composition SDDMM -> row-softmax
  * -> SpMM of the Abstract): for the upstream gradient dO [n_rows, heads, D], per head,
  *   w = softmax over row i of scale * <Q[i], K[j]>,  dW_p = <dO[i], V[j]>,

@@ -39,6 +39,7 @@ EXPORTS = [
     "autosage_row_stats", "autosage_fingerprint", "autosage_validate_csr", "autosage_csr_transpose",
     "autosage_status_string", "autosage_last_error", "autosage_version",
     "autosage_csr_attention_unfused_noalloc", "autosage_csr_attention_backward",
+    "autosage_plan_typed", "autosage_spmm_typed",
 ]
 
 
@@ -72,6 +73,8 @@ def _load():
         "autosage_csr_attention": [CSR, P, P, P, I, I64, I, F, P, I, P, P],
         "autosage_csr_attention_unfused_noalloc": [CSR, P, P, P, I, I64, I, F, P, P],
         "autosage_csr_attention_backward": [CSR, P, P, P, P, I, I64, I, F, P, P, P, P, P],
+        "autosage_plan_typed": [CSR, P, I, I64, I, U, ctypes.POINTER(P), P],
+        "autosage_spmm_typed": [CSR, P, I, P, I64, P, I64, I64, I, P, P],
         "autosage_edge_softmax_aggregate": [CSR, P, P, I, I64, I, P, P, P],
         "autosage_plan": [CSR, I, I64, I, I, U, ctypes.POINTER(P), P],
         "autosage_plan_with_schedule": [CSR, I, I64, I, I, ctypes.POINTER(_Schedule), ctypes.POINTER(P), P],
@@ -299,6 +302,32 @@ def autosage_csr_attention(A: CsrMatrix, Q, K, V, heads: int, scale: float, fuse
     _check(_lib.autosage_csr_attention(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), D, _dt(Q), float(scale),
                                        _ptr(out), int(bool(fused)), _plan_handle(plan), _stream(stream)))
     return out
+
+
+def autosage_plan_typed(A: CsrMatrix, edge_type, num_types: int, F: int, dtype=None, flags: int = 0,
+                        stream=None) -> Plan:
+    """Plan for the multi-relation SpMM (checks the edge types on the GPU)."""
+    torch = _torch()
+    dt = BF16 if dtype == torch.bfloat16 else F32
+    if edge_type.dtype != torch.int32 or not edge_type.is_contiguous():
+        raise TypeError("edge_type must be a contiguous int32 tensor")
+    h = ctypes.c_void_p()
+    _check(_lib.autosage_plan_typed(A.c, _ptr(edge_type), int(num_types), int(F), dt, int(flags), ctypes.byref(h),
+                                    _stream(stream)))
+    return Plan(h.value, OP_SPMM)
+
+
+def autosage_spmm_typed(A: CsrMatrix, edge_type, Z, Y=None, plan: Plan | None = None, stream=None):
+    """Y[i] = sum_p vals[p] Z[edge_type[p], col_idx[p]] with Z [num_types, n_cols, F]."""
+    torch = _torch()
+    if Z.dim() != 3 or not Z.is_contiguous():
+        raise ValueError("Z must be a contiguous [num_types, n_cols, F] tensor")
+    R, _, F = (int(x) for x in Z.shape)
+    if Y is None:
+        Y = torch.empty((A.n_rows, F), dtype=Z.dtype, device=Z.device)
+    _check(_lib.autosage_spmm_typed(A.c, _ptr(edge_type), R, _ptr(Z), F, _ptr(Y), _ld(Y), F, _dt(Z),
+                                    _plan_handle(plan), _stream(stream)))
+    return Y
 
 
 def autosage_csr_attention_backward(A: CsrMatrix, Q, K, V, dO, heads: int, scale: float, dQ=None, dK=None,

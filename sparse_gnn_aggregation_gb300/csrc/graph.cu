@@ -310,6 +310,26 @@ __global__ void transpose_gather_kernel(int64_t nnz, const int32_t *__restrict__
   if (vals_t) vals_t[k] = vals[p];
 }
 
+// ---------------------------------------------------------------- typed edges
+
+// combined[p] = edge_type[p] * n_cols + col_idx[p]: the row of Z that edge p
+// gathers when the relations' feature blocks are stacked. Types outside
+// [0, n_types) are flagged and their index is set to 0.
+__global__ void typed_index_kernel(int64_t nnz, int64_t n_cols, int n_types, const int32_t *__restrict__ col_idx,
+                                   const int32_t *__restrict__ edge_type, int32_t *__restrict__ combined,
+                                   int *__restrict__ err) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < nnz; p += stride) {
+    const int r = edge_type[p];
+    if (r < 0 || r >= n_types) {
+      atomicOr(err, 1);
+      combined[p] = 0;
+    } else {
+      combined[p] = static_cast<int32_t>((int64_t)r * n_cols + col_idx[p]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- probes
 
 __global__ void fill_probe_kernel(void *__restrict__ p, int64_t n, int bf16, unsigned long long seed) {
@@ -482,6 +502,14 @@ cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int
   cudaFreeAsync(counts, s);
   cudaFreeAsync(scan_tmp, s);
   return err;
+}
+
+cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const int32_t *col_idx,
+                               const int32_t *edge_type, int32_t *combined, int *err, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e != cudaSuccess || nnz <= 0) return e;
+  typed_index_kernel<<<grid_for(nnz, 256), 256, 0, s>>>(nnz, n_cols, n_types, col_idx, edge_type, combined, err);
+  return cudaGetLastError();
 }
 
 cudaError_t fill_probe(void *p, int64_t n_elems, DType dt, uint64_t seed, cudaStream_t s) {

@@ -258,10 +258,14 @@ struct autosage_plan_s {
   // A^T position -> A edge (SPMM_T); backward edge buffers and the A^T SpMM plan
   DevBuf t_perm, grad_dw, grad_wt, grad_dst;
   autosage_plan_s *tplan = nullptr;
+  // typed SpMM: number of relations (0: untyped) and the combined gather index
+  int typed = 0;
+  int64_t base_cols = 0;
+  DevBuf typed_idx;
   ~autosage_plan_s() {
     for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
                       &chunk_begin, &partial, &ml, &row_ml, &mp_part, &mp_carry_val,
-                      &mp_carry_row, &scores, &t_perm, &grad_dw, &grad_wt, &grad_dst})
+                      &mp_carry_row, &scores, &t_perm, &grad_dw, &grad_wt, &grad_dst, &typed_idx})
       b->release();
     delete tplan;
   }
@@ -1348,6 +1352,78 @@ autosage_status autosage_csr_attention_backward(const autosage_csr *A, const voi
   cudaError_t e = cudaStreamSynchronize(s);
   delete P;
   if (st == AUTOSAGE_OK && e != cudaSuccess) return cuda_fail(e, "attention backward");
+  return st;
+}
+
+autosage_status autosage_plan_typed(const autosage_csr *A, const int32_t *edge_type, int num_types, int64_t F,
+                                    autosage_dtype dt, unsigned flags, autosage_plan_t *out, void *stream) {
+  if (!out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (num_types < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "num_types must be >= 1");
+  if (A->nnz > 0 && !edge_type) return fail(AUTOSAGE_ERR_INVALID_ARG, "edge_type is NULL");
+  if ((int64_t)num_types * std::max<int64_t>(A->n_cols, 1) >= INT32_MAX)
+    return fail(AUTOSAGE_ERR_UNSUPPORTED, "num_types * n_cols must fit int32");
+  cudaStream_t s = as_stream(stream);
+  DevBuf idx;
+  CUDA_TRY(idx.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(A->nnz, 1)));
+  int *derr = nullptr, herr = 0;
+  CUDA_TRY(cudaMallocAsync(&derr, sizeof(int), s));
+  cudaError_t e = launch_typed_index(A->nnz, A->n_cols, num_types, A->col_idx, edge_type, idx.as<int32_t>(), derr, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&herr, derr, sizeof(int), cudaMemcpyDeviceToHost, s);
+  cudaFreeAsync(derr, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    idx.release();
+    return cuda_fail(e, "typed index");
+  }
+  if (herr) {
+    idx.release();
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "edge_type outside [0, num_types)");
+  }
+  // an ordinary SpMM plan over the stacked blocks: A' has num_types * n_cols columns
+  autosage_csr Ap{A->n_rows, (int64_t)num_types * A->n_cols, A->nnz, A->row_ptr, idx.as<int32_t>(), A->vals};
+  autosage_plan_t P = nullptr;
+  st = autosage_plan(&Ap, AUTOSAGE_OP_SPMM, F, 1, dt, flags, &P, stream);
+  if (!P) {
+    idx.release();
+    return st;
+  }
+  P->typed = num_types;
+  P->base_cols = A->n_cols;
+  P->typed_idx = idx;  // the plan owns the index from here on
+  idx.p = nullptr;
+  idx.bytes = 0;
+  *out = P;
+  return st;
+}
+
+autosage_status autosage_spmm_typed(const autosage_csr *A, const int32_t *edge_type, int num_types, const void *Z,
+                                    int64_t ldz, void *Y, int64_t ldy, int64_t F, autosage_dtype dt,
+                                    autosage_plan_t plan, void *stream) {
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (F < 1 || num_types < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "F and num_types must be >= 1");
+  if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
+  if ((st = check_mat(Z, ldz, F, (int64_t)num_types * A->n_cols, "Z")) != AUTOSAGE_OK) return st;
+  if ((st = check_mat(Y, ldy, F, A->n_rows, "Y")) != AUTOSAGE_OK) return st;
+  if (A->n_rows == 0) return AUTOSAGE_OK;
+  OpArgs a;
+  a.X = Z; a.ldx = ldz; a.Y = Y; a.ldy = ldy;
+  cudaStream_t s = as_stream(stream);
+  if (plan) {
+    if (plan->typed != num_types || plan->base_cols != A->n_cols || plan->n_rows != A->n_rows ||
+        plan->nnz != A->nnz || plan->F != F || (int)plan->dt != (int)dt || plan->op != AUTOSAGE_OP_SPMM)
+      return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan not built by autosage_plan_typed for this call");
+    return run_op(plan, AUTOSAGE_OP_SPMM, a, s);
+  }
+  autosage_plan_t P = nullptr;
+  st = autosage_plan_typed(A, edge_type, num_types, F, dt, AUTOSAGE_PLAN_NO_CACHE, &P, stream);
+  if (st == AUTOSAGE_OK) st = run_op(P, AUTOSAGE_OP_SPMM, a, s);
+  cudaError_t e = cudaStreamSynchronize(s);
+  autosage_plan_destroy(P);
+  if (st == AUTOSAGE_OK && e != cudaSuccess) return cuda_fail(e, "typed SpMM");
   return st;
 }
 
