@@ -556,11 +556,16 @@ def cpu_baseline(graphs, budget_s=15.0, steps=1):
             tot_b += b
         return tot_b, tot_t
 
-    f0 = 1.0 / 2048
-    one_pass(f0)  # warm: features, transpose, thread pool
-    b, t = one_pass(f0)
-    frac = min(1.0, f0 * budget_s / t) if t > 0 else f0
+    frac = 1.0 / 2048
+    one_pass(frac)  # warm: features, transpose, thread pool
     b, t = one_pass(frac)
+    # the time per row falls as the sample grows (fixed costs per call), so
+    # rescale until a pass takes at least half the budget
+    for _ in range(3):
+        if t >= 0.5 * budget_s or frac >= 1.0:
+            break
+        frac = min(1.0, frac * budget_s / max(t, 1e-3))
+        b, t = one_pass(frac)
     return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"a seeded uniform {100 * frac:.2f}% of the rows of each graph for every operation of "
                       f"the step ({b / 1e9:.2f} GB algorithmic, {t:.1f} s)"}

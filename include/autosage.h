@@ -68,15 +68,17 @@ typedef enum {
   AUTOSAGE_SCHED_ROWGROUP = 0,   /* one lane group per row: G feature lanes x E edge lanes */
   AUTOSAGE_SCHED_SPLIT = 1,      /* rows longer than `split` edges are cut into chunks whose
                                     partial results are combined in a fixed order */
-  AUTOSAGE_SCHED_MERGEPATH = 2   /* equal (rows + edges) share per warp along the merge path,
+  AUTOSAGE_SCHED_MERGEPATH = 2,  /* equal (rows + edges) share per warp along the merge path,
                                     carry-out of rows cut at warp boundaries, fixed-order fix-up */
+  AUTOSAGE_SCHED_BINNED = 3      /* SPLIT, with rows taken in order of degree bucket (longest
+                                    first) so the lane groups of a warp get rows of similar length */
 } autosage_sched_kind;
 
 typedef struct {
   int kind;        /* autosage_sched_kind */
   int lanes_f;     /* G: lanes across the feature vector (power of two, 1..32); 0 = auto */
   int lanes_e;     /* E: lanes across edges of one row (power of two, G*E <= 32); 0 = auto */
-  int split;       /* SPLIT: chunk length in edges; MERGEPATH: items per warp; 0 = auto */
+  int split;       /* SPLIT/BINNED: chunk length in edges; MERGEPATH: items per warp; 0 = auto */
 } autosage_schedule;
 
 /* A CSR matrix in device memory. Rows are destinations, col_idx are sources.

@@ -147,6 +147,7 @@ struct ChunkList {
   const int32_t *chunk_begin = nullptr;  // [n_chunks]
   const int32_t *long_rows = nullptr;    // [n_long]
   const int32_t *long_ptr = nullptr;     // [n_long + 1]
+  const int32_t *row_order = nullptr;  // [n_rows] rows in processing order (null: 0, 1, 2, ...)
   int n_chunks = 0;
   int n_long = 0;
   int split = 0;  // 0: no row is cut
@@ -161,8 +162,10 @@ struct Item {
   bool active;
 };
 
-// Work item number idx of a persistent launch: the chunks of cut rows come
-// first (the longest items start earliest), then every row in order.
+// Work item number idx of a launch: the chunks of cut rows come first (the
+// longest items start earliest), then every row, in row_order when the plan
+// has one (degree-binned schedules: rows sorted by degree bucket, longest
+// first, so the lane groups of a warp get rows of similar length).
 __device__ __forceinline__ Item item_at(int64_t idx, int64_t n_rows, const int32_t *row_ptr,
                                         const ChunkList &cl) {
   Item it{0, 0, 0, -1, false};
@@ -174,7 +177,7 @@ __device__ __forceinline__ Item item_at(int64_t idx, int64_t n_rows, const int32
     it.e = (re - it.b > cl.split) ? it.b + cl.split : re;
     it.active = true;
   } else if (idx - cl.n_chunks < n_rows) {
-    const int64_t r = idx - cl.n_chunks;
+    const int64_t r = cl.row_order ? (int64_t)cl.row_order[idx - cl.n_chunks] : idx - cl.n_chunks;
     it.row = r;
     it.b = row_ptr[r];
     it.e = row_ptr[r + 1];

@@ -310,6 +310,25 @@ __global__ void transpose_gather_kernel(int64_t nnz, const int32_t *__restrict__
   if (vals_t) vals_t[k] = vals[p];
 }
 
+// ---------------------------------------------------------------- degree bins
+
+// Sort key of a row for the degree-binned order: 31 - bit_length(degree), so
+// an ascending stable sort puts the longest rows first; rows cut into chunks
+// (degree > split) get 31 and go last (their row items do no work).
+__global__ void degree_key_kernel(int64_t n_rows, const int32_t *__restrict__ row_ptr, int split,
+                                  int32_t *__restrict__ keys, int32_t *__restrict__ vals) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows) return;
+  const int d = row_ptr[r + 1] - row_ptr[r];
+  int key = 31;
+  if (!(split > 0 && d > split)) {
+    const int b = d == 0 ? 0 : 32 - __clz(d);
+    key = 31 - (b < 31 ? b : 31);
+  }
+  keys[r] = key;
+  vals[r] = static_cast<int32_t>(r);
+}
+
 // ---------------------------------------------------------------- typed edges
 
 // combined[p] = edge_type[p] * n_cols + col_idx[p]: the row of Z that edge p
@@ -501,6 +520,33 @@ cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int
   }
   cudaFreeAsync(counts, s);
   cudaFreeAsync(scan_tmp, s);
+  return err;
+}
+
+cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int64_t n_tiles = (n_rows + kSortTile - 1) / kSortTile;
+  int32_t *keys = nullptr, *keys_out = nullptr, *vals = nullptr, *hist = nullptr, *offs = nullptr;
+  void *scan_tmp = nullptr;
+  const size_t nb = sizeof(int32_t) * (size_t)n_rows;
+  const size_t hb = sizeof(int32_t) * (size_t)(256 * n_tiles + 1);
+  cudaError_t err = cudaSuccess;
+  int32_t **bufs[5] = {&keys, &keys_out, &vals, &hist, &offs};
+  const size_t sizes[5] = {nb, nb, nb, hb, hb};
+  for (int i = 0; i < 5 && err == cudaSuccess; ++i) err = cudaMallocAsync(reinterpret_cast<void **>(bufs[i]), sizes[i], s);
+  if (err == cudaSuccess) err = cudaMallocAsync(&scan_tmp, scan_tmp_bytes(256 * n_tiles), s);
+  if (err == cudaSuccess) {
+    degree_key_kernel<<<(unsigned)((n_rows + 255) / 256), 256, 0, s>>>(n_rows, row_ptr, split, keys, vals);
+    // one stable pass over the 5-bit key
+    radix_hist_kernel<<<(unsigned)n_tiles, kSortThreads, 0, s>>>(keys, n_rows, 0, n_tiles, hist);
+    launch_exclusive_scan(hist, offs, 256 * n_tiles, scan_tmp, s);
+    radix_scatter_kernel<<<(unsigned)n_tiles, kSortThreads, 0, s>>>(keys, vals, n_rows, 0, n_tiles, offs, keys_out,
+                                                                     order);
+    err = cudaGetLastError();
+  }
+  for (int i = 0; i < 5; ++i)
+    if (*bufs[i]) cudaFreeAsync(*bufs[i], s);
+  if (scan_tmp) cudaFreeAsync(scan_tmp, s);
   return err;
 }
 

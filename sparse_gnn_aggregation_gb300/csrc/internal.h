@@ -102,6 +102,9 @@ cudaError_t launch_softmax_backward(int64_t n_rows, const int32_t *row_ptr, int 
 // out_a[k, :] = a[perm[k], :], out_b[k, :] = b[perm[k], :] (rows of H floats).
 cudaError_t launch_permute_edges(int64_t nnz, int H, const int32_t *perm, const float *a, const float *b,
                                  float *out_a, float *out_b, cudaStream_t s);
+// Degree-binned row order: rows sorted (stably) by degree bucket, longest first,
+// rows longer than `split` last. order: [n_rows]. Temporaries from cudaMallocAsync.
+cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order, cudaStream_t s);
 // combined[p] = edge_type[p] * n_cols + col_idx[p]; *err (device) gets 1 for a type out of range.
 cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const int32_t *col_idx,
                                const int32_t *edge_type, int32_t *combined, int *err, cudaStream_t s);

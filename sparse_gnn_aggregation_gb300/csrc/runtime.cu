@@ -248,7 +248,7 @@ struct autosage_plan_s {
   const float *k_vals = nullptr;
   DevBuf t_row_ptr, t_col_idx, t_vals;  // A^T when op == SPMM_T
   // split workspace
-  DevBuf long_rows, long_ptr, chunk_row, chunk_begin, partial, ml, row_ml;
+  DevBuf long_rows, long_ptr, chunk_row, chunk_begin, partial, ml, row_ml, row_order;
   ChunkList cl;
   // merge-path workspace
   DevBuf mp_part, mp_carry_val, mp_carry_row;
@@ -264,7 +264,7 @@ struct autosage_plan_s {
   DevBuf typed_idx;
   ~autosage_plan_s() {
     for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
-                      &chunk_begin, &partial, &ml, &row_ml, &mp_part, &mp_carry_val,
+                      &chunk_begin, &partial, &ml, &row_ml, &row_order, &mp_part, &mp_carry_val,
                       &mp_carry_row, &scores, &t_perm, &grad_dw, &grad_wt, &grad_dst, &typed_idx})
       b->release();
     delete tplan;
@@ -298,6 +298,7 @@ const char *sched_name(int kind) {
     case AUTOSAGE_SCHED_ROWGROUP: return "rowgroup";
     case AUTOSAGE_SCHED_SPLIT: return "split";
     case AUTOSAGE_SCHED_MERGEPATH: return "mergepath";
+    case AUTOSAGE_SCHED_BINNED: return "binned";
   }
   return "?";
 }
@@ -392,7 +393,7 @@ autosage_status build_mergepath(autosage_plan_s *P, int items, int64_t width, cu
 // Build the workspace of a schedule for plan P (P->sched set).
 autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
   for (DevBuf *b : {&P->long_rows, &P->long_ptr, &P->chunk_row, &P->chunk_begin, &P->partial,
-                    &P->ml, &P->row_ml, &P->mp_part, &P->mp_carry_val, &P->mp_carry_row})
+                    &P->ml, &P->row_ml, &P->row_order, &P->mp_part, &P->mp_carry_val, &P->mp_carry_row})
     b->release();
   P->cl = ChunkList{};
   P->mp_warps = 0;
@@ -407,12 +408,18 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
     // longest run of edges one lane sums serially (edge lanes taken as 1 when automatic)
     const int64_t lanes_e = P->sched.E > 0 ? P->sched.E : 1;
     int64_t run = P->maxdeg;
-    if (P->sched.kind == AUTOSAGE_SCHED_SPLIT) run = std::min<int64_t>(run, P->sched.split);
+    if (P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED)
+      run = std::min<int64_t>(run, P->sched.split);
     if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) run = std::min<int64_t>(run, P->sched.split);
     P->comp = run / lanes_e > 512;
   }
-  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT) {
+  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED) {
     st = build_split(P, P->sched.split, s);
+    if (st == AUTOSAGE_OK && P->sched.kind == AUTOSAGE_SCHED_BINNED && P->k_rows > 0) {
+      CUDA_TRY(P->row_order.alloc(sizeof(int32_t) * (size_t)P->k_rows));
+      CUDA_TRY(build_row_order(P->k_rows, P->k_row_ptr, P->sched.split, P->row_order.as<int32_t>(), s));
+      P->cl.row_order = P->row_order.as<int32_t>();
+    }
   } else if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
     if (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)
       return fail(AUTOSAGE_ERR_UNSUPPORTED, "merge-path schedule is SpMM only");
@@ -637,7 +644,7 @@ double estimate(const DeviceInfo &dev, const RowStats &st, autosage_op op, DType
   const double groups = (double)std::max(1, dev.sms) * 48.0 * (32.0 / lanes_per_item);
   const double lat = 1.2e-6;  // one dependent gather round trip
   double steps = 0, longest = 0;
-  int64_t split = sc.kind == AUTOSAGE_SCHED_SPLIT ? sc.split : 0;
+  int64_t split = (sc.kind == AUTOSAGE_SCHED_SPLIT || sc.kind == AUTOSAGE_SCHED_BINNED) ? sc.split : 0;
   for (int b = 0; b < 32; ++b) {
     const double cnt = (double)st.ints[8 + b];
     if (cnt == 0) continue;
@@ -665,7 +672,8 @@ double estimate(const DeviceInfo &dev, const RowStats &st, autosage_op op, DType
   const double t_lat = steps * lat / par;
   const double t_tail = longest * lat;
   double launches = 1;
-  if (sc.kind == AUTOSAGE_SCHED_SPLIT && st.ints[6] > 0) launches += (op == AUTOSAGE_OP_SOFTMAX ? 3 : 1);
+  if ((sc.kind == AUTOSAGE_SCHED_SPLIT || sc.kind == AUTOSAGE_SCHED_BINNED) && st.ints[6] > 0)
+    launches += (op == AUTOSAGE_OP_SOFTMAX ? 3 : 1);
   if (sc.kind == AUTOSAGE_SCHED_MERGEPATH) launches += 1;
   if (op == AUTOSAGE_OP_ATTN_UNFUSED) launches += 2;
   return std::max(t_bw, t_lat) + t_tail + launches * 3e-6;
@@ -719,7 +727,7 @@ autosage_status make_plan_shell(const autosage_csr *A, autosage_op op, int64_t F
 
 // Probe buffers shaped like the op's real arguments (never the caller's data).
 struct ProbeBufs {
-  DevBuf X, Y, Y2, Q, K, S;
+  DevBuf X, Y, Y2, Q, K, S, flush;
   OpArgs a;
   int64_t out_elems = 0;
   bool out_is_S = false;
@@ -774,6 +782,14 @@ autosage_status make_probe_bufs(const autosage_plan_s *P, ProbeBufs &pb, cudaStr
       pb.out_elems = P->n_rows * W;
       break;
   }
+  // a buffer twice the L2 size, overwritten before every timed run so probes
+  // see the cold-cache behaviour the operations meet in a real step
+  if (e == cudaSuccess) {
+    int dev = 0, l2 = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    e = pb.flush.alloc((size_t)std::max(l2, 1 << 20) * 2);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "probe buffers");
   return AUTOSAGE_OK;
 }
@@ -790,6 +806,7 @@ autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &
   for (int r = 0; r <= reps && st == AUTOSAGE_OK; ++r) {
     if (P->op == AUTOSAGE_OP_SOFTMAX)
       cudaMemcpyAsync(pb.Y.p, pb.S.p, (size_t)pb.out_elems * 4, cudaMemcpyDeviceToDevice, s);
+    if (pb.flush.p) cudaMemsetAsync(pb.flush.p, r & 0xff, pb.flush.bytes, s);
     cudaEventRecord(e0, s);
     st = run_op(P, P->op, a, s);
     cudaEventRecord(e1, s);
@@ -846,6 +863,12 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
         if (maxd <= split) continue;
         Sched sp{AUTOSAGE_SCHED_SPLIT, G, E, split};
         out.push_back({sp, estimate(dev, st, P->op, P->dt, P->F, sh.H, sp, g)});
+      }
+      // degree-binned order pays off when lengths vary widely (coefficient of variation > 1)
+      if (st.cv > 1.0 && P->op != AUTOSAGE_OP_SOFTMAX) {
+        const int split = maxd > 128 ? 128 : (int)std::max<int64_t>(maxd, 1);
+        Sched bn{AUTOSAGE_SCHED_BINNED, G, E, split};
+        out.push_back({bn, estimate(dev, st, P->op, P->dt, P->F, sh.H, bn, g) * 0.97});
       }
       if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && G * E == 32) {
         for (int items : {256, 1024}) {
@@ -929,7 +952,7 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
   if (!out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!sched) return fail(AUTOSAGE_ERR_INVALID_ARG, "sched is NULL");
-  if (sched->kind < AUTOSAGE_SCHED_ROWGROUP || sched->kind > AUTOSAGE_SCHED_MERGEPATH)
+  if (sched->kind < AUTOSAGE_SCHED_ROWGROUP || sched->kind > AUTOSAGE_SCHED_BINNED)
     return fail(AUTOSAGE_ERR_INVALID_ARG, "bad schedule kind");
   if ((sched->lanes_f && !is_pow2(sched->lanes_f)) || (sched->lanes_e && !is_pow2(sched->lanes_e)) ||
       sched->lanes_f > 32 || sched->lanes_e > 32 || sched->lanes_f * std::max(1, sched->lanes_e) > 32)
@@ -940,7 +963,8 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
   P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split};
-  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT && P->sched.split == 0) P->sched.split = 1024;
+  if ((P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED) && P->sched.split == 0)
+    P->sched.split = 1024;
   if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH && P->sched.split == 0) P->sched.split = 512;
   if (P->sched.kind == AUTOSAGE_SCHED_ROWGROUP) P->sched.split = 0;
   if (op == AUTOSAGE_OP_ATTN_BACKWARD) {
@@ -1038,7 +1062,7 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
         if (same_sched(t.sc, x)) return true;
       return false;
     };
-    for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH})
+    for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH, AUTOSAGE_SCHED_BINNED})
       for (const Candidate &c : cands)
         if (c.sc.kind == kind) {
           top.push_back(c);
@@ -1555,6 +1579,7 @@ autosage_status autosage_cache_load(const char *path) {
     if (kind == "rowgroup") e.sched.kind = AUTOSAGE_SCHED_ROWGROUP;
     else if (kind == "split") e.sched.kind = AUTOSAGE_SCHED_SPLIT;
     else if (kind == "mergepath") e.sched.kind = AUTOSAGE_SCHED_MERGEPATH;
+    else if (kind == "binned") e.sched.kind = AUTOSAGE_SCHED_BINNED;
     else {
       ++bad;
       continue;

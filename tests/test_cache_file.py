@@ -44,6 +44,7 @@ def test_wrong_header_rejected(tmp_path, sga):
     "no-tab-here split 16 2 512 0.1\n",
     "key\tsplit 16 2\n",                       # truncated
     "key\twarp 16 2 512 0.1\n",                # unknown schedule
+    "key\tbinned 16 2 0 0.1\n",                # binned schedule without a chunk length
     "key\trowgroup 3 1 0 0.1\n",               # lanes not a power of two
     "key\tsplit 16 4 0 0.1\n",                 # split schedule without a chunk length
     "key\trowgroup 16 4 0 0.1 extra\n",        # trailing field

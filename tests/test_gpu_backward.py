@@ -43,8 +43,9 @@ def test_backward_tiny_er():
 
 
 @pytest.mark.parametrize("H,D", [(2, 16), (8, 8), (3, 32)])
-@pytest.mark.parametrize("schedule", [None, dict(kind=sga.SCHED_ROWGROUP), dict(kind=sga.SCHED_SPLIT, split=16)],
-                         ids=["auto", "rowgroup", "split16"])
+@pytest.mark.parametrize("schedule", [None, dict(kind=sga.SCHED_ROWGROUP), dict(kind=sga.SCHED_SPLIT, split=16),
+                                      dict(kind=sga.SCHED_BINNED, split=16)],
+                         ids=["auto", "rowgroup", "split16", "binned16"])
 def test_backward_skewed(H, D, schedule):
     run(synth.rmat_skew(13, seed=5), H, D, 1 / np.sqrt(D), 3, schedule=schedule)
 

@@ -38,6 +38,7 @@ SCHEDULES = [
     ("rowgroup-e4", dict(kind=sga.SCHED_ROWGROUP, lanes_e=4)),
     ("split-8", dict(kind=sga.SCHED_SPLIT, split=8)),
     ("split-64-e2", dict(kind=sga.SCHED_SPLIT, split=64, lanes_e=2)),
+    ("binned-32", dict(kind=sga.SCHED_BINNED, split=32)),
 ]
 SPMM_SCHEDULES = SCHEDULES + [
     ("mergepath-32", dict(kind=sga.SCHED_MERGEPATH, split=32)),
@@ -162,7 +163,7 @@ def test_sddmm_bf16(skew):
 # ---------------------------------------------------------------- softmax
 
 @pytest.mark.parametrize("heads", [1, 2, 3, 8])
-@pytest.mark.parametrize("name,spec", SCHEDULES[:1] + SCHEDULES[3:4], ids=["default", "split-8"])
+@pytest.mark.parametrize("name,spec", SCHEDULES[:1] + SCHEDULES[3:4] + SCHEDULES[5:6], ids=["default", "split-8", "binned-32"])
 def test_row_softmax(skew, heads, name, spec):
     g = skew
     A = mat(g)
@@ -189,7 +190,7 @@ def test_attention_tiny_er(tiny, fused, name, spec):
 
 @pytest.mark.parametrize("heads,D", [(2, 16), (4, 8), (8, 64), (3, 32), (2, 12)])
 @pytest.mark.parametrize("fused", [True, False])
-@pytest.mark.parametrize("name,spec", SCHEDULES[:1] + SCHEDULES[3:5], ids=["default", "split-8", "split-64-e2"])
+@pytest.mark.parametrize("name,spec", SCHEDULES[:1] + SCHEDULES[3:6], ids=["default", "split-8", "split-64-e2", "binned-32"])
 def test_attention_multihead_skewed(skew, heads, D, fused, name, spec):
     g = skew
     A = mat(g)
@@ -250,7 +251,7 @@ def edge_case_graphs():
 
 
 @pytest.mark.parametrize("name,g", edge_case_graphs(), ids=[e[0] for e in edge_case_graphs()])
-@pytest.mark.parametrize("sched", ["default", "split", "mergepath"])
+@pytest.mark.parametrize("sched", ["default", "split", "mergepath", "binned"])
 def test_edge_cases(name, g, sched):
     A = mat(g)
     F = 6
@@ -258,7 +259,7 @@ def test_edge_cases(name, g, sched):
     Q = synth.normal(g.n_rows, F, 11, synth.STREAM_Q)
     K = synth.normal(g.n_cols, F, 11, synth.STREAM_K)
     spec = {"default": None, "split": dict(kind=sga.SCHED_SPLIT, split=2),
-            "mergepath": dict(kind=sga.SCHED_MERGEPATH, split=3)}[sched]
+            "mergepath": dict(kind=sga.SCHED_MERGEPATH, split=3), "binned": dict(kind=sga.SCHED_BINNED, split=2)}[sched]
     plan = make_plan(A, sga.OP_SPMM, F, spec)
     Y = sga.autosage_spmm(A, dev(X), plan=plan)
     assert_close(to_np(Y), oracle.spmm(g.row_ptr, g.col_idx, g.vals, X), TOL_F32, f"{name} spmm")
