@@ -1054,22 +1054,26 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
       best_est = cands[0].est;
     }
   } else {
-    // the best-estimated candidate of each schedule family, then the next best
-    // overall up to six, plus the guardrail default
+    // probes: the best-estimated candidate of each family and lane count, then
+    // the next best overall up to ten, plus the guardrail default
     std::vector<Candidate> top;
     auto have = [&](const Sched &x) {
       for (const Candidate &t : top)
         if (same_sched(t.sc, x)) return true;
       return false;
     };
-    for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH, AUTOSAGE_SCHED_BINNED})
-      for (const Candidate &c : cands)
-        if (c.sc.kind == kind) {
-          top.push_back(c);
-          break;
-        }
+    // the estimate ranks lane counts poorly, so every (family, feature lanes)
+    // pair sends its best candidate to the probes
+    for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH, AUTOSAGE_SCHED_BINNED}) {
+      std::vector<int> seen_g;
+      for (const Candidate &c : cands) {
+        if (c.sc.kind != kind || std::find(seen_g.begin(), seen_g.end(), c.sc.G) != seen_g.end()) continue;
+        seen_g.push_back(c.sc.G);
+        top.push_back(c);
+      }
+    }
     for (const Candidate &c : cands) {
-      if ((int)top.size() >= 6) break;
+      if ((int)top.size() >= 10) break;
       if (!have(c.sc)) top.push_back(c);
     }
     if (!have(default_sched())) top.push_back({default_sched(), -1});
