@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
   const Lanes L(G, E);
   const int g = L.g;
   const int base_lane = L.slot * L.GE + L.e * G;  // lane 0 of this edge lane's segment
-  constexpr int U = B < 4 ? B : 4;
+  // loads of the whole batch in flight when a lane holds at most two fragments
+  constexpr int U = NV <= 2 ? B : (B < 4 ? B : 4);
   __shared__ int s_items;
   const ItemQueue queue(n_rows, cl, ipb, &s_items);
   int64_t idx;
@@ -131,11 +132,14 @@ __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
     // edges of this edge lane: p = it.b + e + E * t; batches of B consecutive t
     const int first = it.b + L.e;
     const int n_mine = it.e > first ? (it.e - first + E - 1) / E : 0;
+    // one load brings a batch's column indices (lane j holding edge j's); the
+    // next batch's indices are requested while this batch's rows are in flight
+    int next_col = (g < B && g < n_mine) ? ld_stream_i32(col_idx + first + g * E) : 0;
     for (int t0 = 0; t0 < n_mine; t0 += B) {
       const int nb = min(B, n_mine - t0);
-      // one load brings the batch's column indices, lane j holding edge j's
       const int pj = first + (t0 + g) * E;
-      const int my_col = g < nb ? ld_stream_i32(col_idx + pj) : 0;
+      const int my_col = next_col;
+      next_col = (g < B && t0 + B + g < n_mine) ? ld_stream_i32(col_idx + first + (t0 + B + g) * E) : 0;
       float part[B];
 #pragma unroll
       for (int j0 = 0; j0 < B; j0 += U) {
