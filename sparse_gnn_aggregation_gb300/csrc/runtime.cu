@@ -794,8 +794,17 @@ autosage_status make_probe_bufs(const autosage_plan_s *P, ProbeBufs &pb, cudaStr
   return AUTOSAGE_OK;
 }
 
+// Host-side fault injection for tests of the guardrail (no GPU fault):
+// AUTOSAGE_FAULT=probe_fail makes every probe report a failure,
+// AUTOSAGE_FAULT=verify_fail makes every spot check report a mismatch.
+bool fault(const char *name) {
+  const char *f = getenv("AUTOSAGE_FAULT");
+  return f && strcmp(f, name) == 0;
+}
+
 // Time one schedule: 1 warm-up, then `reps` timed runs; median in ms.
 autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &ms, cudaStream_t s) {
+  if (fault("probe_fail")) return fail(AUTOSAGE_ERR_PROBE, "probe failure injected (AUTOSAGE_FAULT=probe_fail)");
   std::vector<float> t;
   cudaEvent_t e0, e1;
   CUDA_TRY(cudaEventCreate(&e0));
@@ -1124,6 +1133,7 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
           cudaFreeAsync(cnt, s);
           cudaStreamSynchronize(s);
         }
+        if (fault("verify_fail")) h = 1;
         if (h != 0) {
           log_line("plan key=%s reject %s G=%d E=%d split=%d mismatches=%llu", key.c_str(),
                    sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, h);
