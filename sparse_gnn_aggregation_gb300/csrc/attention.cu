@@ -278,7 +278,7 @@ cudaError_t attention_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const T *Q, const T *K, const float *scores,
                          const T *V, int64_t ld, float scale, T *O, const ChunkList &cl,
                          float *part_acc, float *part_ml, cudaStream_t s) {
-  const int ipb = items_per_block_for(g.G * g.E);
+  const int ipb = items_per_block_for(g.G * g.E, g.G);
   const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
 #define AUTOSAGE_ATTN(NVV, GIV, ONEG)                                                               \

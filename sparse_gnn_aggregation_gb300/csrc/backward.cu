@@ -118,7 +118,7 @@ cudaError_t launch_softmax_backward(int64_t n_rows, const int32_t *row_ptr, int 
                                     cudaStream_t s) {
   const bool divides = (32 % H) == 0;
   const int GS = 32;
-  const int ipb = items_per_block_for(GS);
+  const int ipb = items_per_block_for(GS, 1);
   const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
     if (divides)

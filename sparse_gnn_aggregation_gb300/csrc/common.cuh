@@ -14,10 +14,12 @@ constexpr int kBlock = 256;  // threads per block of the gather kernels
 // ---------------------------------------------------------------- lane groups
 //
 // A warp is cut into 32 / (G*E) groups; each group owns one work item (a row
-// or a chunk of a row). Inside a group, lane l = e*G + g: g in [0, G) walks
-// the feature vector in VW-element fragments (fragment c = g + k*G for
-// k < NV), e in [0, E) walks the item's edges (p = begin + e, e + E, ...).
-// Feature lanes are adjacent, so one gathered row is read by adjacent lanes.
+// or a chunk of a row) at a time. Inside a group, lane l = e*G + g: g in
+// [0, G) walks the feature vector in VW-element fragments (NV fragments per
+// lane: interleaved, fragment g + k*G, or, where a lane should stay inside
+// one attention head, consecutive, fragment g*NV + k), e in [0, E) walks the
+// item's edges (p = begin + e, e + E, ...). Feature lanes are adjacent, so
+// one gathered row is read by adjacent lanes.
 struct Lanes {
   int G, E, GE;
   int lane, g, e, slot;
@@ -31,10 +33,6 @@ struct Lanes {
     slot = lane / GE;
     group_mask = (GE == 32) ? FULL : (((1u << GE) - 1u) << (slot * GE));
     sub_mask = (G == 32) ? FULL : (((1u << G) - 1u) << (slot * GE + e * G));
-  }
-  // Global index of this lane's group.
-  __device__ __forceinline__ int64_t group_index(int64_t block_base) const {
-    return (block_base + (threadIdx.x >> 5)) * (32 / GE) + slot;
   }
 };
 
@@ -213,8 +211,12 @@ struct ItemQueue {
 };
 
 // Items per block: a few per lane group, so blocks stay short enough for the
-// block scheduler to balance them across SMs.
-inline int items_per_block_for(int GE) { return (kBlock / 32) * (32 / GE) * 4; }
+// block scheduler to balance them across SMs. Whole-warp groups over wide
+// rows (G >= 16 of 32 lanes) take 16 each, other groups 8 (measured on the
+// R-MAT scale-20 step: fewer, longer blocks pay off where items are heavy).
+inline int items_per_block_for(int GE, int G) {
+  return (kBlock / 32) * (32 / GE) * ((GE == 32 && G >= 16) ? 16 : 8);
+}
 
 __device__ __forceinline__ int64_t items_per_block(int GE) { return (kBlock / 32) * (32 / GE); }
 

@@ -1157,7 +1157,7 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
   }
   P->sched = best;
   P->probe_ms = best_ms;
-  P->est_ms = best_est * 1e3;
+  P->est_ms = best_est >= 0 ? best_est * 1e3 : -1;
   st = build_workspace(P, s);
   if (st != AUTOSAGE_OK && !same_sched(best, default_sched())) {
     P->sched = default_sched();

@@ -152,7 +152,7 @@ cudaError_t launch_row_softmax(int64_t n_rows, const int32_t *row_ptr, int H, fl
   if (divides) {
     GS = H < 8 ? 8 : H;
   }
-  const int ipb = items_per_block_for(GS);
+  const int ipb = items_per_block_for(GS, 1);
   const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
     if (divides)

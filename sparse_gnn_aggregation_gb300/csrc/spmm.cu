@@ -328,7 +328,7 @@ template <typename T, int VW>
 cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
                     const float *vals, const T *X, int64_t ldx, T *Y, int64_t ldy,
                     const ChunkList &cl, float *partial, cudaStream_t s) {
-  const int ipb = items_per_block_for(g.G * g.E);
+  const int ipb = items_per_block_for(g.G * g.E, g.G);
   const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
   if (grid > 0) {
 #define AUTOSAGE_SPMM_K(NVV, CMP)                                                                 \
