@@ -134,7 +134,18 @@ autosage_status choose_geom(DType dt, int H, int64_t D, std::initializer_list<Ma
   g.batched = false;
   if (H == 1) {
     g.batched = g.G >= 4;  // batches of 4 (G = 4) or 8 edges
-  } else if (need_head_reduce) {
+  } else if (!need_head_reduce) {
+    // per-head weights only (SpMM): with four or more slots per lane,
+    // consecutive fragments keep a lane in one head, so each edge needs one
+    // weight per lane instead of one per slot (measured: faster at 4 slots,
+    // slower at 2, where interleaved lanes coalesce better)
+    if (g.NV >= 4 && g.NV <= g.cph && g.cph % g.NV == 0) {
+      g.fs = g.NV;
+      g.ks = 1;
+    } else {
+      g.one = false;
+    }
+  } else {
     if (!is_pow2(g.cph))
       return fail(AUTOSAGE_ERR_UNSUPPORTED, "multi-head reduction needs D/VW a power of two");
     if (g.NV <= g.cph) {  // consecutive fragments per lane, all in one head

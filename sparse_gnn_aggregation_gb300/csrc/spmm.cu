@@ -42,9 +42,11 @@ __device__ __forceinline__ void accum(float &acc, float &comp, float w, float x)
 }
 
 // Edge weights of U edges p, p + E, ... for every fragment slot.
+// Slots share one weight when there is one head or every slot of the lane
+// lies in the same head (`one`); otherwise each slot loads its head's weight.
 template <int U, int NV>
 __device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx,
-                                             const float *__restrict__ vals, int H, int es,
+                                             const float *__restrict__ vals, int H, int es, bool one,
                                              const int (&head)[NV], int p, int E, int (&c)[U],
                                              float (&w)[U][NV]) {
 #pragma unroll
@@ -54,8 +56,9 @@ __device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx
     if (vals == nullptr) {
 #pragma unroll
       for (int k = 0; k < NV; ++k) w[u][k] = 1.f;
-    } else if (H == 1) {
-      const float x = ld_stream_f32(vals + (int64_t)(p + u * E) * es);
+    } else if (H == 1 || one) {
+      const float x = H == 1 ? ld_stream_f32(vals + (int64_t)(p + u * E) * es)
+                             : __ldg(vals + (int64_t)(p + u * E) * es + head[0]);
 #pragma unroll
       for (int k = 0; k < NV; ++k) w[u][k] = x;
     } else {
@@ -71,33 +74,33 @@ __device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx
 // so each iteration waits on one memory round trip, not two.
 template <typename T, int VW, int NV, int U, bool COMP>
 __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx,
-                                             const float *__restrict__ vals, int H, int es,
+                                             const float *__restrict__ vals, int H, int es, bool one,
                                              const int (&head)[NV], const T *__restrict__ X,
-                                             int64_t ldx, int nfrag, int g, int G, int E, int p0,
+                                             int64_t ldx, int nfrag, const int (&frag)[NV], int E, int p0,
                                              int pe, float (&acc)[NV][VW], float (&comp)[NV][VW]) {
   int p = p0;
   if constexpr (U > 1) {
     if (p + (U - 1) * E < pe) {
       int c[U];
       float w[U][NV];
-      load_weights<U, NV>(col_idx, vals, H, es, head, p, E, c, w);
+      load_weights<U, NV>(col_idx, vals, H, es, one, head, p, E, c, w);
       while (true) {
         Frag<T, VW> f[U][NV];
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
           for (int k = 0; k < NV; ++k)
-            if (g + k * G < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)(g + k * G) * VW);
+            if (frag[k] < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)frag[k] * VW);
         const int pn = p + U * E;
         const bool more = pn + (U - 1) * E < pe;
         int cn[U];
         float wn[U][NV];
-        if (more) load_weights<U, NV>(col_idx, vals, H, es, head, pn, E, cn, wn);
+        if (more) load_weights<U, NV>(col_idx, vals, H, es, one, head, pn, E, cn, wn);
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
           for (int k = 0; k < NV; ++k)
-            if (g + k * G < nfrag)
+            if (frag[k] < nfrag)
 #pragma unroll
               for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[u][k], f[u][k].get(v));
         p = pn;
@@ -118,14 +121,14 @@ __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx
     for (int k = 0; k < NV; ++k)
       w[k] = vals == nullptr ? 1.f
              : H == 1        ? __ldg(vals + (int64_t)p * es)
-                             : __ldg(vals + (int64_t)p * es + head[k]);
+                             : __ldg(vals + (int64_t)p * es + head[one ? 0 : k]);
     Frag<T, VW> f[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (g + k * G < nfrag) f[k].load(X + (int64_t)c * ldx + (int64_t)(g + k * G) * VW);
+      if (frag[k] < nfrag) f[k].load(X + (int64_t)c * ldx + (int64_t)frag[k] * VW);
 #pragma unroll
     for (int k = 0; k < NV; ++k)
-      if (g + k * G < nfrag)
+      if (frag[k] < nfrag)
 #pragma unroll
         for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[k], f[k].get(v));
   }
@@ -150,14 +153,14 @@ template <typename T, int VW, int NV, bool COMP>
 __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const float *__restrict__ vals, int H, int es, int cph, const T *__restrict__ X, int64_t ldx,
-    T *__restrict__ Y, int64_t ldy, int nfrag, int G, int E, ChunkList cl, int ipb,
-    float *__restrict__ partial) {
+    T *__restrict__ Y, int64_t ldy, int nfrag, int G, int E, int fs, int ks, bool one, ChunkList cl,
+    int ipb, float *__restrict__ partial) {
   const Lanes L(G, E);
-  int head[NV];
+  int frag[NV], head[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    const int c = L.g + k * G;
-    head[k] = (H > 1 && c < nfrag) ? c / cph : 0;
+    frag[k] = L.g * fs + k * ks;
+    head[k] = (H > 1 && frag[k] < nfrag) ? frag[k] / cph : 0;
   }
   __shared__ int s_items;
   const ItemQueue queue(n_rows, cl, ipb, &s_items);
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
     float acc[NV][VW], comp[NV][VW];
     zero(acc);
     zero(comp);
-    gather_edges<T, VW, NV, unroll_for<NV, VW>(), COMP>(col_idx, vals, H, es, head, X, ldx, nfrag, L.g, G,
+    gather_edges<T, VW, NV, unroll_for<NV, VW>(), COMP>(col_idx, vals, H, es, one, head, X, ldx, nfrag, frag,
                                                          E, it.b + L.e, it.e, acc, comp);
     reduce_edge_lanes(acc, L.group_mask, G, L.GE);
     if (!it.active || L.e != 0) continue;
@@ -175,12 +178,12 @@ __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
       T *y = Y + it.row * ldy;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (L.g + k * G < nfrag) store_frag<T, VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+        if (frag[k] < nfrag) store_frag<T, VW>(y + (int64_t)frag[k] * VW, acc[k]);
     } else {
       float *y = partial + (int64_t)it.chunk * nfrag * VW;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (L.g + k * G < nfrag) store_partial<VW>(y + (int64_t)(L.g + k * G) * VW, acc[k]);
+        if (frag[k] < nfrag) store_partial<VW>(y + (int64_t)frag[k] * VW, acc[k]);
     }
   }
 }
@@ -251,13 +254,17 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
   const Lanes L(G, E);       // G * E == 32: one group per warp
   const int2 s0 = part[w], s1 = part[w + 1];
   const int head[NV] = {};
+  int frag[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) frag[k] = L.g + k * G;
   constexpr int U = unroll_for<NV, VW>();
   for (int i = s0.x; i < s1.x; ++i) {
     const int b = max(row_ptr[i], s0.y), e = row_ptr[i + 1];
     float acc[NV][VW], comp[NV][VW];
     zero(acc);
     zero(comp);
-    gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, e, acc, comp);
+    gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, true, head, X, ldx, nfrag, frag, E, b + L.e, e, acc,
+                                     comp);
     reduce_edge_lanes(acc, FULL, G, 32);
     if (L.e == 0) {
       T *y = Y + (int64_t)i * ldy;
@@ -275,8 +282,8 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
       float acc[NV][VW], comp[NV][VW];
       zero(acc);
       zero(comp);
-      gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, head, X, ldx, nfrag, L.g, G, E, b + L.e, s1.y, acc,
-                                       comp);
+      gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, true, head, X, ldx, nfrag, frag, E, b + L.e, s1.y,
+                                       acc, comp);
       reduce_edge_lanes(acc, FULL, G, 32);
       if (L.e == 0) {
         float *cv = carry_val + w * (int64_t)nfrag * VW;
@@ -333,8 +340,8 @@ cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const
   if (grid > 0) {
 #define AUTOSAGE_SPMM_K(NVV, CMP)                                                                 \
   spmm_rows_kernel<T, VW, NVV, CMP><<<(unsigned)grid, kBlock, 0, s>>>(                          \
-      n_rows, row_ptr, col_idx, vals, g.H, g.es, g.cph, X, ldx, Y, ldy, g.nfrag, g.G, g.E, cl, ipb, \
-      partial)
+      n_rows, row_ptr, col_idx, vals, g.H, g.es, g.cph, X, ldx, Y, ldy, g.nfrag, g.G, g.E, g.fs, g.ks,  \
+      g.one, cl, ipb, partial)
 #define AUTOSAGE_SPMM_NV(NVV)          \
   if (g.comp) AUTOSAGE_SPMM_K(NVV, true); \
   else AUTOSAGE_SPMM_K(NVV, false);
