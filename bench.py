@@ -125,17 +125,16 @@ def attn_bytes(n, nnz, H, D, s, fused):
 
 
 def attn_backward_bytes(n, m, nnz, H, D, s):
-    """Algorithmic bytes of one CSR-attention backward: the sum over its steps
-    (two SDDMMs, softmax, softmax backward, SpMM for dQ, the reorder of two edge
-    arrays, and the two SpMMs over A^T for dK and dV)."""
+    """Algorithmic bytes of one CSR-attention backward: the one pass over the
+    rows of A (CSR arrays, Q and dO rows once per row, K and V rows gathered
+    per edge, dQ written, scores and dW written and read back per edge and
+    head, the A^T position of each edge read, w and dS written in A^T order)
+    and the two SpMMs over A^T for dV and dK (per-head weights, gathered dO
+    and Q rows, outputs)."""
     W = H * D
-    sddmm = 4 * (n + 1) + 4 * nnz + n * W * s + nnz * W * s + 4 * nnz * H
-    softmax = 3 * 4 * nnz * H
-    softmax_bwd = 4 * 4 * nnz * H
-    spmm_q = 4 * (n + 1) + 4 * nnz + 4 * nnz * H + nnz * W * s + n * W * s
-    permute = 4 * nnz + 4 * 4 * nnz * H
+    rows = 4 * (n + 1) + 4 * nnz + 3 * n * W * s + 2 * nnz * W * s + 4 * 4 * nnz * H + 4 * nnz + 2 * 4 * nnz * H
     spmm_t = 4 * (m + 1) + 4 * nnz + 4 * nnz * H + nnz * W * s + m * W * s
-    return 2 * sddmm + softmax + softmax_bwd + spmm_q + permute + 2 * spmm_t
+    return rows + 2 * spmm_t
 
 
 def op_list(graphs, only=None):
@@ -151,7 +150,7 @@ def op_list(graphs, only=None):
     ops.append(("attn_fused/rmat/H8D64", "attn_fused", "rmat", HEAD_DIM))
     ops.append(("attn_unfused/rmat/H8D64", "attn_unfused", "rmat", HEAD_DIM))
     if only:
-        ops = [o for o in ops if only in o[0]]
+        ops = [o for o in ops if any(w in o[0] for w in only.split(","))]
     return ops
 
 
@@ -349,7 +348,7 @@ def run_ours(args):
 
     # rows beyond the step (SURVEY "next"): CSR-attention backward on the same graph
     next_rows = {}
-    if not args.no_next and (not args.only or "backward" in args.only):
+    if not args.no_next and (not args.only or "backward" in args.only.split(",")):
         g = graphs["rmat"]
         A = mats["rmat"]
         W = HEADS * HEAD_DIM
@@ -377,7 +376,7 @@ def run_ours(args):
             "ms": round(ms, 4), "GBps": round(b / ms / 1e6, 1), "frac_of_hbm_peak": round(b / ms / 1e6 / peak_gbs, 4),
             "bytes": int(b), "dtype": "bf16 in/out, f32 accumulate", "plan": bplan.describe()}
         del bq, bk, bv, bo, outs_b, bplan
-    if not args.no_next and (not args.only or "typed" in args.only):
+    if not args.no_next and (not args.only or "typed" in args.only.split(",")):
         # multi-relation SpMM (RGCN-style): 4 relations, F = 64, fp32
         g = graphs["rmat"]
         A = mats["rmat"]
@@ -548,7 +547,7 @@ def cpu_baseline(graphs, budget_s=15.0, steps=1):
             samples[key] = (rows, int(deg.sum()))
         return samples[key]
 
-    def one_pass(frac):
+    def one_pass(frac, per_op=None):
         tot_b, tot_t = 0.0, 0.0
         for key, kind, gname, F in ops:
             g = graphs[gname]
@@ -573,23 +572,28 @@ def cpu_baseline(graphs, budget_s=15.0, steps=1):
             else:
                 oracle.csr_attention(g.row_ptr, g.col_idx, X, X, X, HEADS, 0.125, rows=rows)
                 b = attn_bytes(rows.size, enn, HEADS, HEAD_DIM, 2, kind == "attn_fused")
-            tot_t += time.perf_counter() - t0
+            dt = time.perf_counter() - t0
+            if per_op is not None:
+                per_op[key] = {"GBps": round(b / dt / 1e9, 3), "s": round(dt, 4)}
+            tot_t += dt
             tot_b += b
         return tot_b, tot_t
 
     frac = 1.0 / 2048
     one_pass(frac)  # warm: features, transpose, thread pool
-    b, t = one_pass(frac)
+    per_op = {}
+    b, t = one_pass(frac, per_op)
     # the time per row falls as the sample grows (fixed costs per call), so
     # rescale until a pass takes at least half the budget
     for _ in range(3):
         if t >= 0.5 * budget_s or frac >= 1.0:
             break
         frac = min(1.0, frac * budget_s / max(t, 1e-3))
-        b, t = one_pass(frac)
+        b, t = one_pass(frac, per_op)
     return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"a seeded uniform {100 * frac:.2f}% of the rows of each graph for every operation of "
-                      f"the step ({b / 1e9:.2f} GB algorithmic, {t:.1f} s)"}
+                      f"the step ({b / 1e9:.2f} GB algorithmic, {t:.1f} s)",
+            "per_op": per_op}
 
 
 def run_reference(args):
@@ -624,7 +628,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows measured beyond the step")
-    ap.add_argument("--only", default=None, help="run only operations whose key contains this text")
+    ap.add_argument("--only", default=None, help="run only operations whose key contains one of these comma-separated texts "
+                         "(backward, typed: the rows measured beyond the step)")
     ap.add_argument("--scale", type=int, default=20, help="R-MAT scale (20 is the benchmark workload)")
     ap.add_argument("--cache", default=None, help="plan cache file: loaded if present, saved after planning")
     args = ap.parse_args()

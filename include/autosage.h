@@ -157,8 +157,10 @@ autosage_status autosage_spmm_typed(const autosage_csr *A, const int32_t *edge_t
  *   dS_p = w_p (dW_p - sum_q w_q dW_q),
  *   dQ[i] = scale * sum_p dS_p K[j],  dK[j] = scale * sum_{p: col(p)=j} dS_p Q[i],
  *   dV[j] = sum_{p: col(p)=j} w_p dO[i].
- * The weights are recomputed from Q and K (SDDMM + softmax), dW is an SDDMM, dQ an SpMM
- * over A, dK and dV SpMMs over A^T with the edge arrays reordered into A^T's edge order.
+ * One pass over the rows of A recomputes the scores, keeps an online softmax state and
+ * produces dW, the row sums and dQ (each K and V row gathered once per edge); it writes
+ * w and scale * dS into the edge order of A^T, where two SpMMs give dV and dK.
+ * heads * D may be at most 256 fragments of 16 bytes (fp32 1024, bf16 2048) when aligned.
  * Q, dO, dQ have n_rows rows; K, V, dK, dV have n_cols rows; all [., heads, D] of type dt,
  * contiguous. plan: built for AUTOSAGE_OP_ATTN_BACKWARD with F = D (it holds A^T, the
  * permutation and the edge buffers); NULL builds a temporary plan inside the call, which

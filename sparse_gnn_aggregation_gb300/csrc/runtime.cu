@@ -266,8 +266,9 @@ struct autosage_plan_s {
   int64_t mp_warps = 0;
   // unfused attention scores (backward: the softmax weights)
   DevBuf scores;
-  // A^T position -> A edge (SPMM_T); backward edge buffers and the A^T SpMM plan
-  DevBuf t_perm, grad_dw, grad_wt, grad_dst;
+  // A^T position -> A edge (SPMM_T); backward: A edge -> A^T position, edge
+  // buffers (dW scratch, w and dS in A^T order) and the A^T SpMM plan
+  DevBuf t_perm, t_inv, grad_dw, grad_wt, grad_dst;
   autosage_plan_s *tplan = nullptr;
   // typed SpMM: number of relations (0: untyped) and the combined gather index
   int typed = 0;
@@ -276,7 +277,7 @@ struct autosage_plan_s {
   ~autosage_plan_s() {
     for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
                       &chunk_begin, &partial, &ml, &row_ml, &row_order, &mp_part, &mp_carry_val,
-                      &mp_carry_row, &scores, &t_perm, &grad_dw, &grad_wt, &grad_dst, &typed_idx})
+                      &mp_carry_row, &scores, &t_perm, &t_inv, &grad_dw, &grad_wt, &grad_dst, &typed_idx})
       b->release();
     delete tplan;
   }
@@ -331,7 +332,7 @@ OpShape op_shape(autosage_op op, int64_t F, int H) {
     case AUTOSAGE_OP_ATTN: return {H, F, true, 8};
     case AUTOSAGE_OP_ATTN_UNFUSED: return {H, F, true, 16};
     case AUTOSAGE_OP_SOFTMAX: return {H, 1, false, 16};
-    case AUTOSAGE_OP_ATTN_BACKWARD: return {H, F, true, 16};
+    case AUTOSAGE_OP_ATTN_BACKWARD: return {H, F, true, 8};
   }
   return {1, F, false, 16};
 }
@@ -382,6 +383,12 @@ autosage_status build_split(autosage_plan_s *P, int split, cudaStream_t s) {
   const bool heads_op = P->op == AUTOSAGE_OP_ATTN || P->op == AUTOSAGE_OP_ATTN_UNFUSED ||
                         P->op == AUTOSAGE_OP_ATTN_BACKWARD;
   const int64_t width = P->F * (heads_op ? P->H : 1);
+  if (P->op == AUTOSAGE_OP_ATTN_BACKWARD) {
+    // per chunk: the (A, B) feature sums, (m, l, sum e dW) per head and the cut row's index
+    CUDA_TRY(P->partial.alloc(sizeof(float) * (size_t)std::max<int64_t>(C * (2 * width + 3 * P->H + 1), 1)));
+    CUDA_TRY(P->row_ml.alloc(sizeof(float) * (size_t)std::max<int64_t>(n_long * P->H * 3, 1)));
+    return AUTOSAGE_OK;
+  }
   if (P->op != AUTOSAGE_OP_SDDMM && P->op != AUTOSAGE_OP_SOFTMAX)
     CUDA_TRY(P->partial.alloc(sizeof(float) * (size_t)std::max<int64_t>(C * width, 1)));
   const int Hs = (P->op == AUTOSAGE_OP_SOFTMAX || heads_op) ? P->H : 1;
@@ -577,34 +584,16 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
       const autosage_plan_s *T = P->tplan;
       if (!T) return fail(AUTOSAGE_ERR_INVALID_ARG, "backward plan lacks its A^T part");
       const int64_t ld = P->H * P->F;
-      float *W = P->scores.as<float>(), *dS = P->grad_dw.as<float>();
-      // weights: SDDMM(Q, K) * scale, then the row softmax
-      st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}}, P->sched.G, P->sched.E, true, 16, g);
+      // scores, softmax, dW, D and dQ in one pass over the rows of A; w and
+      // scale * dS land in the edge order of A^T
+      st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}, {a.X, ld}, {a.dO, ld}, {a.dQ, ld}},
+                       P->sched.G, P->sched.E, true, 8, g);
       if (st != AUTOSAGE_OK) return st;
-      e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, ld, a.K, ld, a.alpha, W, cl, s);
-      if (e == cudaSuccess)
-        e = launch_row_softmax(P->k_rows, P->k_row_ptr, P->H, W, cl, P->ml.as<float>(), P->row_ml.as<float>(), s);
-      // dW = SDDMM(dO, V); dS = scale * W * (dW - rowsum(W * dW)) in place
-      if (e == cudaSuccess) {
-        st = choose_geom(P->dt, P->H, P->F, {{a.dO, ld}, {a.X, ld}}, P->sched.G, P->sched.E, true, 16, g);
-        if (st != AUTOSAGE_OK) return st;
-        e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.dO, ld, a.X, ld, 1.f, dS, cl, s);
-      }
-      if (e == cudaSuccess)
-        e = launch_softmax_backward(P->k_rows, P->k_row_ptr, P->H, W, dS, a.alpha, cl, P->ml.as<float>(),
-                                    P->row_ml.as<float>(), s);
-      // dQ = SpMM(A; dS, K)
-      if (e == cudaSuccess) {
-        st = choose_geom(P->dt, P->H, P->F, {{a.K, ld}, {a.dQ, ld}}, P->sched.G, P->sched.E, false, 16, g);
-        if (st != AUTOSAGE_OK) return st;
-        g.comp = P->comp;
-        e = launch_spmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, dS, a.K, ld, a.dQ, ld, cl,
-                        P->partial.as<float>(), s);
-      }
-      // W and dS in the edge order of A^T, then dV = SpMM(A^T; W, dO), dK = SpMM(A^T; dS, Q)
-      if (e == cudaSuccess)
-        e = launch_permute_edges(P->nnz, P->H, T->t_perm.as<int32_t>(), W, dS, P->grad_wt.as<float>(),
-                                 P->grad_dst.as<float>(), s);
+      e = launch_attention_backward(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.K, a.X, a.dO, ld, a.alpha,
+                                    a.dQ, P->scores.as<float>(), P->grad_dw.as<float>(), P->t_inv.as<int32_t>(),
+                                    P->grad_wt.as<float>(), P->grad_dst.as<float>(), cl,
+                                    P->partial.as<float>(), P->row_ml.as<float>(), s);
+      // dV = SpMM(A^T; w, dO), dK = SpMM(A^T; scale * dS, Q)
       if (e == cudaSuccess) {
         st = choose_geom(P->dt, P->H, P->F, {{a.dO, ld}, {a.dV, ld}}, T->sched.G, T->sched.E, false, 16, g);
         if (st != AUTOSAGE_OK) return st;
@@ -853,17 +842,31 @@ struct Candidate {
   double est;
 };
 
+// Geometry of G feature lanes x E edge lanes for the op's width, as the
+// candidate list and the estimate see it (fragment width from the row size).
+// False when a lane would need more fragment slots than the kernels have.
+bool cand_geom(const autosage_plan_s *P, int G, int E, Geom &g) {
+  const OpShape sh = op_shape(P->op, P->F, P->H);
+  const int s = dtype_size(P->dt);
+  int vb = 16;
+  while (vb > s && (P->F * s) % vb) vb >>= 1;
+  const int64_t nfrag = std::max<int64_t>(1, (P->F * sh.H * s) / vb);
+  if (G < 1 || E < 1 || G * E > 32 || G > std::min<int64_t>(32, pow2ceil(nfrag))) return false;
+  g = Geom{};
+  g.dt = P->dt; g.H = sh.H; g.D = sh.D; g.VW = vb / s; g.nfrag = (int)nfrag; g.G = G; g.E = E;
+  g.NV = pow2ceil((nfrag + G - 1) / G);
+  return g.NV <= sh.nv_max;
+}
+
 // Candidate schedules for the op and its statistics.
 std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *P, const RowStats &st) {
   std::vector<Candidate> out;
   const OpShape sh = op_shape(P->op, P->F, P->H);
   // lanes across features from the width (what choose_geom would pick)
   const int s = dtype_size(P->dt);
-  const int64_t Fb = P->F * sh.H * s;
   int vb = 16;
   while (vb > s && (P->F * s) % vb) vb >>= 1;
   const int64_t nfrag = std::max<int64_t>(1, (P->F * sh.H * s) / vb);
-  (void)Fb;
   std::vector<int> Gs;
   const int G0 = std::min(32, pow2ceil(nfrag));
   Gs.push_back(G0);
@@ -874,9 +877,7 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
     for (int E = 1; G * E <= 32; E <<= 1) {
       if (P->op == AUTOSAGE_OP_SOFTMAX && E > 1) break;
       Geom g{};
-      g.dt = P->dt; g.H = sh.H; g.D = sh.D; g.VW = vb / s; g.nfrag = (int)nfrag; g.G = G; g.E = E;
-      g.NV = pow2ceil((nfrag + G - 1) / G);
-      if (g.NV > sh.nv_max) continue;
+      if (!cand_geom(P, G, E, g)) continue;
       Sched rg{AUTOSAGE_SCHED_ROWGROUP, G, E, 0};
       out.push_back({rg, estimate(dev, st, P->op, P->dt, P->F, sh.H, rg, g)});
       for (int split : {128, 512, 2048, 8192}) {
@@ -899,6 +900,60 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
     }
   }
   std::stable_sort(out.begin(), out.end(), [](const Candidate &a, const Candidate &b) { return a.est < b.est; });
+  return out;
+}
+
+// Neighbours of a schedule for the probes' local refinement: half or twice
+// the edge lanes, half or twice the feature lanes, a quarter or four times
+// the chunk length (merge path: the items per warp), and the other chunked
+// family (split <-> binned) with the same lanes and chunk length. Automatic
+// lanes (0) are first resolved the way the kernels resolve them.
+std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *P, const RowStats &st,
+                                  const Sched &b) {
+  std::vector<Candidate> out;
+  const OpShape sh = op_shape(P->op, P->F, P->H);
+  const int64_t maxd = st.ints[2];
+  const bool softmax = P->op == AUTOSAGE_OP_SOFTMAX;
+  int G = b.G, E = b.E;
+  if (G <= 0 || E <= 0) {
+    const int s = dtype_size(P->dt);
+    int vb = 16;
+    while (vb > s && (P->F * s) % vb) vb >>= 1;
+    const int64_t nfrag = std::max<int64_t>(1, (P->F * sh.H * s) / vb);
+    if (G <= 0) G = std::min(32, pow2ceil(nfrag));
+    if (E <= 0) E = std::max(1, std::min(32 / G, 8));
+  }
+  auto add = [&](Sched x) {
+    Geom g{};
+    if (!cand_geom(P, x.G, x.E, g)) return;
+    if (softmax && x.E != 1) return;
+    if (x.kind == AUTOSAGE_SCHED_MERGEPATH) {
+      if (x.G * x.E != 32 || (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)) return;
+      if (x.split < 64 || x.split > 16384) return;
+    } else if (x.kind == AUTOSAGE_SCHED_SPLIT) {
+      if (x.split < 16 || x.split >= maxd) return;
+    } else if (x.kind == AUTOSAGE_SCHED_BINNED) {
+      if (softmax || x.split < 16) return;
+    } else {
+      x.split = 0;
+    }
+    for (const Candidate &c : out)
+      if (same_sched(c.sc, x)) return;
+    out.push_back({x, estimate(dev, st, P->op, P->dt, P->F, sh.H, x, g)});
+  };
+  for (int e2 : {E / 2, E * 2}) {
+    if (e2 < 1 || e2 > 32) continue;
+    // merge path keeps whole warps: the feature lanes follow the edge lanes
+    add(Sched{b.kind, b.kind == AUTOSAGE_SCHED_MERGEPATH ? 32 / e2 : G, e2, b.split});
+  }
+  if (b.kind != AUTOSAGE_SCHED_MERGEPATH && !softmax)
+    for (int g2 : {G / 2, G * 2})
+      if (g2 >= 1) add(Sched{b.kind, g2, E, b.split});
+  if (b.kind != AUTOSAGE_SCHED_ROWGROUP)
+    for (int s2 : {b.split / 4, b.split * 4}) add(Sched{b.kind, G, E, s2});
+  if (b.kind == AUTOSAGE_SCHED_SPLIT) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split});
+  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_SPLIT, G, E, b.split});
+  if (b.kind == AUTOSAGE_SCHED_ROWGROUP && maxd > 128) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, 128});
   return out;
 }
 
@@ -936,6 +991,10 @@ autosage_status build_backward_plan(autosage_plan_s *P, const Sched &sc, cudaStr
   }
   delete P->tplan;
   P->tplan = T;
+  // where each edge of A sits in A^T: the backward writes w and dS there directly
+  CUDA_TRY(P->t_inv.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(P->nnz, 1)));
+  CUDA_TRY(launch_invert_perm(P->nnz, T->t_perm.as<int32_t>(), P->t_inv.as<int32_t>(), s));
+  CUDA_TRY(cudaStreamSynchronize(s));
   return AUTOSAGE_OK;
 }
 
@@ -1119,18 +1178,18 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
       }
     }
     int ok_count = 0;
-    for (const Candidate &c : top) {
+    auto probe_one = [&](const Candidate &c) {
       P->sched = c.sc;
       if (build_workspace(P, s) != AUTOSAGE_OK) {
         log_line("plan key=%s skip %s G=%d E=%d split=%d workspace: %s", key.c_str(), sched_name(c.sc.kind),
                  c.sc.G, c.sc.E, c.sc.split, g_last_error.c_str());
-        continue;
+        return;
       }
       double ms = 0;
       if (probe_time(P, pb, 5, ms, s) != AUTOSAGE_OK) {
         log_line("plan key=%s skip %s G=%d E=%d split=%d probe: %s", key.c_str(), sched_name(c.sc.kind),
                  c.sc.G, c.sc.E, c.sc.split, g_last_error.c_str());
-        continue;
+        return;
       }
       if (verify && have_ref && !same_sched(c.sc, default_sched())) {
         unsigned long long *cnt = nullptr, h = 1;
@@ -1148,7 +1207,7 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
         if (h != 0) {
           log_line("plan key=%s reject %s G=%d E=%d split=%d mismatches=%llu", key.c_str(),
                    sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, h);
-          continue;
+          return;
         }
       }
       ++ok_count;
@@ -1159,6 +1218,21 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
         best = c.sc;
         best_est = c.est;
       }
+    };
+    for (const Candidate &c : top) probe_one(c);
+    // local refinement: the estimate ranks edge lanes and chunk lengths
+    // poorly, so the neighbours of the fastest schedule are probed too, and
+    // again around each new fastest one (at most four rounds)
+    std::vector<Sched> tried;
+    for (const Candidate &c : top) tried.push_back(c.sc);
+    for (int round = 0; round < 4 && best_ms >= 0; ++round) {
+      const Sched centre = best;
+      for (const Candidate &c : neighbours(dev, P, rs, centre)) {
+        if (std::any_of(tried.begin(), tried.end(), [&](const Sched &t) { return same_sched(t, c.sc); })) continue;
+        tried.push_back(c.sc);
+        probe_one(c);
+      }
+      if (same_sched(best, centre)) break;
     }
     cudaGetLastError();  // a failed candidate must not poison later calls
     if (ok_count == 0) {
