@@ -276,10 +276,12 @@ __global__ void __launch_bounds__(kBlock) attention_fixup_kernel(ChunkList cl, i
 template <typename T, int VW>
 cudaError_t attention_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const T *Q, const T *K, const float *scores,
-                         const T *V, int64_t ld, float scale, T *O, const ChunkList &cl,
+                         const T *V, int64_t ld, float scale, T *O, const ChunkList &cl_in,
                          float *part_acc, float *part_ml, cudaStream_t s) {
-  const int ipb = items_per_block_for(g.G * g.E, g.G);
-  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
+  const Deal dl = deal_items(cl_in, n_rows, g.G * g.E, g.G);
+  const ChunkList &cl = dl.cl;
+  const int ipb = dl.ipb;
+  const int64_t grid = dl.grid;
   if (grid > 0) {
 #define AUTOSAGE_ATTN(NVV, GIV, ONEG)                                                               \
   attention_kernel<T, VW, NVV, GIV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                       \

@@ -38,6 +38,13 @@ __host__ __device__ constexpr int bwd_unroll() {
   return NV * VW * (int)sizeof(T) <= 32 ? 2 : 1;
 }
 
+// Blocks per SM the register budget is sized for: lanes holding at most 16
+// bytes of a row fit three 256-thread blocks (85 registers), wider ones two.
+template <typename T, int VW, int NV>
+constexpr int bwd_min_blocks() {
+  return NV * VW * (int)sizeof(T) <= 16 ? 3 : 2;
+}
+
 // Per-chunk state layout in `part`: [n_chunks][2][width] for (A, B), then
 // [n_chunks][H][3] for (m, l, sum e dW), then [n_chunks] cut-row indices.
 struct BwdPart {
@@ -59,10 +66,10 @@ __device__ __forceinline__ BwdPart bwd_part(float *part, int64_t n_chunks, int64
 // own head. R lanes share a head; the first of them (g % R == 0) writes that
 // head's per-edge values.
 template <typename T, int VW, int NV, bool ONE>
-__global__ void __launch_bounds__(kBlock, 2) attn_bwd_rows_kernel(
+__global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_rows_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ dO,
-    int64_t ld, float scale, int H, int cph, int R, int nfrag, int G, int E, int fs, int ks,
+    int64_t ld, float scale, int H, int es, int cph, int R, int nfrag, int G, int E, int fs, int ks,
     T *__restrict__ dQ, float *__restrict__ S, float *__restrict__ dW, const int32_t *__restrict__ inv,
     float *__restrict__ Wt, float *__restrict__ dSt, ChunkList cl, int ipb, float *__restrict__ part) {
   constexpr int NG = ONE ? 1 : NV;
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kBlock, 2) attn_bwd_rows_kernel(
 #pragma unroll
             for (int j = 0; j < NG; ++j)
               if (valid[j]) {
-                const int64_t i = (int64_t)(p + u * E) * H + head[j];
+                const int64_t i = (int64_t)(p + u * E) * es + head[j];
                 S[i] = s[u][j];
                 dW[i] = dw[u][j];
               }
@@ -303,10 +310,10 @@ __global__ void __launch_bounds__(kBlock, 2) attn_bwd_rows_kernel(
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
           if (!valid[j]) continue;
-          const int64_t i = (int64_t)p * H + head[j];
+          const int64_t i = (int64_t)p * es + head[j];
           const float w = __expf(S[i] - m[j]) * il[j];
-          __stcs(Wt + t * H + head[j], w);
-          __stcs(dSt + t * H + head[j], scale * w * (dW[i] - dd[j]));
+          __stcs(Wt + t * es + head[j], w);
+          __stcs(dSt + t * es + head[j], scale * w * (dW[i] - dd[j]));
         }
       }
     }
@@ -369,7 +376,7 @@ __global__ void __launch_bounds__(kBlock) attn_bwd_fixup_kernel(ChunkList cl, in
 
 // w and dS of the chunks' edges (one warp per chunk), in the edge order of A^T.
 __global__ void __launch_bounds__(kBlock) attn_bwd_chunks_kernel(
-    const int32_t *__restrict__ row_ptr, ChunkList cl, int H, float scale, const float *__restrict__ S,
+    const int32_t *__restrict__ row_ptr, ChunkList cl, int H, int es, float scale, const float *__restrict__ S,
     const float *__restrict__ dW, const int32_t *__restrict__ inv, const float *__restrict__ part,
     int64_t width, const float *__restrict__ row_st, float *__restrict__ Wt, float *__restrict__ dSt) {
   const int64_t c = (int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5);
@@ -386,10 +393,11 @@ __global__ void __launch_bounds__(kBlock) attn_bwd_chunks_kernel(
     const int64_t p = i / H;
     const int h = static_cast<int>(i - p * H);
     const float *rs = row_st + (j * H + h) * 3;
-    const float w = __expf(__ldcs(S + i) - rs[0]) * rs[1];
+    const int64_t q = p * es + h;
+    const float w = __expf(__ldcs(S + q) - rs[0]) * rs[1];
     const int64_t t = inv[p];
-    __stcs(Wt + t * H + h, w);
-    __stcs(dSt + t * H + h, scale * w * (__ldcs(dW + i) - rs[2]));
+    __stcs(Wt + t * es + h, w);
+    __stcs(dSt + t * es + h, scale * w * (__ldcs(dW + q) - rs[2]));
   }
 }
 
@@ -402,15 +410,17 @@ __global__ void invert_perm_kernel(int64_t n, const int32_t *__restrict__ perm, 
 
 template <typename T, int VW>
 cudaError_t attn_bwd_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
-                        const T *Q, const T *K, const T *V, const T *dO, int64_t ld, float scale, T *dQ,
-                        float *S, float *dW, const int32_t *inv, float *Wt, float *dSt, const ChunkList &cl,
+                        const T *Q, const T *K, const T *V, const T *dO, int64_t ld, int es, float scale, T *dQ,
+                        float *S, float *dW, const int32_t *inv, float *Wt, float *dSt, const ChunkList &cl_in,
                         float *part, float *row_st, cudaStream_t s) {
-  const int ipb = items_per_block_for(g.G * g.E, g.G);
-  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
+  const Deal dl = deal_items(cl_in, n_rows, g.G * g.E, g.G);
+  const ChunkList &cl = dl.cl;
+  const int ipb = dl.ipb;
+  const int64_t grid = dl.grid;
   if (grid > 0) {
 #define AUTOSAGE_BWD(NVV, ONEG)                                                                            \
   attn_bwd_rows_kernel<T, VW, NVV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                               \
-      n_rows, row_ptr, col_idx, Q, K, V, dO, ld, scale, g.H, g.cph, g.R, g.nfrag, g.G, g.E, g.fs, g.ks, dQ, \
+      n_rows, row_ptr, col_idx, Q, K, V, dO, ld, scale, g.H, es, g.cph, g.R, g.nfrag, g.G, g.E, g.fs, g.ks, dQ, \
       S, dW, inv, Wt, dSt, cl, ipb, part)
 #define AUTOSAGE_BWD_NV(NVV)           \
   if (g.one) AUTOSAGE_BWD(NVV, true);  \
@@ -433,7 +443,7 @@ cudaError_t attn_bwd_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, c
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const unsigned cgrid = (unsigned)((cl.n_chunks + kBlock / 32 - 1) / (kBlock / 32));
-    attn_bwd_chunks_kernel<<<cgrid, kBlock, 0, s>>>(row_ptr, cl, g.H, scale, S, dW, inv, part,
+    attn_bwd_chunks_kernel<<<cgrid, kBlock, 0, s>>>(row_ptr, cl, g.H, es, scale, S, dW, inv, part,
                                                      (int64_t)g.nfrag * VW, row_st, Wt, dSt);
     return cudaGetLastError();
   }
@@ -444,8 +454,8 @@ cudaError_t attn_bwd_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, c
 
 cudaError_t launch_attention_backward(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                                       const int32_t *col_idx, const void *Q, const void *K, const void *V,
-                                      const void *dO, int64_t ld, float scale, void *dQ, float *S, float *dW,
-                                      const int32_t *inv, float *Wt, float *dSt, const ChunkList &cl,
+                                      const void *dO, int64_t ld, int es, float scale, void *dQ, float *S,
+                                      float *dW, const int32_t *inv, float *Wt, float *dSt, const ChunkList &cl,
                                       float *part, float *row_st, cudaStream_t s) {
   if (g.dt == DType::F32) {
     auto q = static_cast<const float *>(Q);
@@ -454,9 +464,9 @@ cudaError_t launch_attention_backward(const Geom &g, int64_t n_rows, const int32
     auto go = static_cast<const float *>(dO);
     auto o = static_cast<float *>(dQ);
     switch (g.VW) {
-      case 4: return attn_bwd_vw<float, 4>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
-      case 2: return attn_bwd_vw<float, 2>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
-      case 1: return attn_bwd_vw<float, 1>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 4: return attn_bwd_vw<float, 4>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 2: return attn_bwd_vw<float, 2>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 1: return attn_bwd_vw<float, 1>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
     }
   } else {
     auto q = static_cast<const __nv_bfloat16 *>(Q);
@@ -465,10 +475,10 @@ cudaError_t launch_attention_backward(const Geom &g, int64_t n_rows, const int32
     auto go = static_cast<const __nv_bfloat16 *>(dO);
     auto o = static_cast<__nv_bfloat16 *>(dQ);
     switch (g.VW) {
-      case 8: return attn_bwd_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
-      case 4: return attn_bwd_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
-      case 2: return attn_bwd_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
-      case 1: return attn_bwd_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 8: return attn_bwd_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 4: return attn_bwd_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 2: return attn_bwd_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
+      case 1: return attn_bwd_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, q, k, v, go, ld, es, scale, o, S, dW, inv, Wt, dSt, cl, part, row_st, s);
     }
   }
   return cudaErrorInvalidValue;

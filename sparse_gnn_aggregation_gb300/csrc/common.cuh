@@ -149,6 +149,7 @@ struct ChunkList {
   int n_chunks = 0;
   int n_long = 0;
   int split = 0;  // 0: no row is cut
+  int chunk_run = 0;  // chunks per block of a launch (set by deal_items)
 };
 
 // One work item: (row, edge begin, edge end, chunk slot or -1 for a whole row).
@@ -185,18 +186,25 @@ __device__ __forceinline__ Item item_at(int64_t idx, int64_t n_rows, const int32
   return it;
 }
 
-// Items of a launch are dealt to blocks in runs of `ipb`; inside a block the
-// lane groups take the block's items one at a time from a shared counter, so
-// a group that drew short rows goes on with the next item instead of idling
-// until the block's longest row ends. Groups of one warp may take different
-// numbers of items; all their shuffles use group or sub-group masks.
+// Items of a launch are dealt to blocks: first the chunks of cut rows, in
+// runs of `cl.chunk_run` (a few per lane group: chunks are the longest
+// items), then the rows in runs of `ipb`. Inside a block the lane groups take the block's
+// items one at a time from a shared counter, so a group that drew short rows
+// goes on with the next item instead of idling until the block's longest row
+// ends. Groups of one warp may take different numbers of items; all their
+// shuffles use group or sub-group masks.
 struct ItemQueue {
   int64_t base, end;
   int *counter;
   __device__ __forceinline__ ItemQueue(int64_t n_rows, const ChunkList &cl, int ipb, int *shared_counter) {
-    base = (int64_t)blockIdx.x * ipb;
-    const int64_t n_items = n_rows + cl.n_chunks;
-    end = base + ipb < n_items ? base + ipb : n_items;
+    // selects, not branches: the branchy form cost the gather kernels registers
+    const int run = cl.chunk_run > 0 ? cl.chunk_run : ipb;
+    const unsigned chunk_blocks = (static_cast<unsigned>(cl.n_chunks) + run - 1) / run;  // n_chunks < 2^31
+    const bool in_chunks = blockIdx.x < chunk_blocks;
+    base = in_chunks ? (int64_t)blockIdx.x * run : cl.n_chunks + (int64_t)(blockIdx.x - chunk_blocks) * ipb;
+    const int64_t lim = in_chunks ? (int64_t)cl.n_chunks : n_rows + cl.n_chunks;
+    const int64_t stop = base + (in_chunks ? run : ipb);
+    end = stop < lim ? stop : lim;
     counter = shared_counter;
     if (threadIdx.x == 0) *counter = 0;
     __syncthreads();
@@ -218,7 +226,27 @@ inline int items_per_block_for(int GE, int G) {
   return (kBlock / 32) * (32 / GE) * ((GE == 32 && G >= 16) ? 16 : 8);
 }
 
-__device__ __forceinline__ int64_t items_per_block(int GE) { return (kBlock / 32) * (32 / GE); }
+// The deal of one launch over n_rows rows with lane groups of GE lanes: the
+// chunk list with its chunk run set, the row run, and the grid that covers
+// both (blocks of chunks first). A chunk block gives each lane group about
+// 512 edges (one chunk of 512 or more, four of 128, at most as many chunks
+// as a row block gives it rows): a block of long chunks would otherwise run
+// long after the rest of the grid has finished.
+struct Deal {
+  ChunkList cl;
+  int ipb;
+  int64_t grid;
+};
+inline Deal deal_items(const ChunkList &cl, int64_t n_rows, int GE, int G) {
+  Deal d{cl, items_per_block_for(GE, G), 0};
+  const int groups = (kBlock / 32) * (32 / GE);
+  int per_group = cl.split > 0 ? 512 / cl.split : 1;
+  per_group = per_group < 1 ? 1 : (per_group > d.ipb / groups ? d.ipb / groups : per_group);
+  d.cl.chunk_run = groups * per_group;
+  const int64_t chunk_blocks = (cl.n_chunks + d.cl.chunk_run - 1) / d.cl.chunk_run;
+  d.grid = chunk_blocks + (n_rows + d.ipb - 1) / d.ipb;
+  return d;
+}
 
 
 }  // namespace autosage

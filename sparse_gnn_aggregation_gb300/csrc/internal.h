@@ -94,15 +94,17 @@ cudaError_t build_chunk_lists(int64_t n_rows, const int32_t *row_ptr, int split,
 cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int32_t *row_ptr,
                           const int32_t *col_idx, const float *vals, int32_t *row_ptr_t,
                           int32_t *col_idx_t, float *vals_t, int32_t *perm, cudaStream_t s);
-// CSR-attention backward over the edges of A, one pass per row: dQ, and the
+// CSR-attention backward over the edges of A, one pass per row, for the g.H
+// heads that Q, K, V, dO, dQ point at (row stride ld elements): dQ, and the
 // softmax weights w and score gradients scale * dS written into the edge order
-// of A^T (Wt, dSt: [nnz * H]; inv[p] = position of edge p in A^T).
-// S, dW: [nnz * H] scratch (scores and dW). part: per chunk 2 * H * D + 3 * H
-// fp32 plus one int32; row_st: [n_long * H * 3] fp32 (cut rows only).
+// of A^T (Wt, dSt: edge p's head h at p * es + h; inv[p] = position of edge
+// p in A^T). S, dW: scratch with the same layout (scores and dW). part: per
+// chunk 2 * H * D + 3 * H fp32 plus one int32; row_st: [n_long * H * 3] fp32
+// (cut rows only).
 cudaError_t launch_attention_backward(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                                       const int32_t *col_idx, const void *Q, const void *K, const void *V,
-                                      const void *dO, int64_t ld, float scale, void *dQ, float *S, float *dW,
-                                      const int32_t *inv, float *Wt, float *dSt, const ChunkList &cl,
+                                      const void *dO, int64_t ld, int es, float scale, void *dQ, float *S,
+                                      float *dW, const int32_t *inv, float *Wt, float *dSt, const ChunkList &cl,
                                       float *part, float *row_st, cudaStream_t s);
 // inv[perm[k]] = k for a permutation of n entries.
 cudaError_t launch_invert_perm(int64_t n, const int32_t *perm, int32_t *inv, cudaStream_t s);

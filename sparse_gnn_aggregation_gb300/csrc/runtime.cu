@@ -589,9 +589,9 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
       st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}, {a.X, ld}, {a.dO, ld}, {a.dQ, ld}},
                        P->sched.G, P->sched.E, true, 8, g);
       if (st != AUTOSAGE_OK) return st;
-      e = launch_attention_backward(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.K, a.X, a.dO, ld, a.alpha,
-                                    a.dQ, P->scores.as<float>(), P->grad_dw.as<float>(), P->t_inv.as<int32_t>(),
-                                    P->grad_wt.as<float>(), P->grad_dst.as<float>(), cl,
+      e = launch_attention_backward(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.K, a.X, a.dO, ld, P->H,
+                                    a.alpha, a.dQ, P->scores.as<float>(), P->grad_dw.as<float>(),
+                                    P->t_inv.as<int32_t>(), P->grad_wt.as<float>(), P->grad_dst.as<float>(), cl,
                                     P->partial.as<float>(), P->row_ml.as<float>(), s);
       // dV = SpMM(A^T; w, dO), dK = SpMM(A^T; scale * dS, Q)
       if (e == cudaSuccess) {
@@ -998,7 +998,10 @@ autosage_status build_backward_plan(autosage_plan_s *P, const Sched &sc, cudaStr
   return AUTOSAGE_OK;
 }
 
-Sched default_backward_sched() { return Sched{AUTOSAGE_SCHED_SPLIT, 0, 0, 128}; }
+// The backward's schedule: rows in degree-binned order, rows longer than 512
+// edges cut (measured on the R-MAT scale-20 graph, H = 8, D = 64, bf16: 15.4 ms
+// against 16.8 ms for split rows of 128 in plain order).
+Sched default_backward_sched() { return Sched{AUTOSAGE_SCHED_BINNED, 0, 0, 512}; }
 
 }  // namespace
 
@@ -1072,7 +1075,7 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
   autosage_plan_s *P = nullptr;
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
-  if (op == AUTOSAGE_OP_ATTN_BACKWARD) {  // fixed schedule: cut rows longer than 128 edges
+  if (op == AUTOSAGE_OP_ATTN_BACKWARD) {  // fixed schedule (no probes)
     st = build_backward_plan(P, default_backward_sched(), s);
     if (st != AUTOSAGE_OK) {
       delete P;

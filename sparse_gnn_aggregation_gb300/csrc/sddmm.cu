@@ -202,9 +202,11 @@ cudaError_t launch_batched(const Geom &g, int64_t grid, int ipb, int64_t n_rows,
 template <typename T, int VW>
 cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
                      const T *Q, int64_t ldq, const T *K, int64_t ldk, float alpha, float *S,
-                     const ChunkList &cl, cudaStream_t s) {
-  const int ipb = items_per_block_for(g.G * g.E, g.G);
-  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
+                     const ChunkList &cl_in, cudaStream_t s) {
+  const Deal dl = deal_items(cl_in, n_rows, g.G * g.E, g.G);
+  const ChunkList &cl = dl.cl;
+  const int ipb = dl.ipb;
+  const int64_t grid = dl.grid;
   if (grid <= 0) return cudaSuccess;
   // batched transpose-reduction: single head, 16-byte fragments, 2..32 lanes
   if constexpr (sizeof(T) * VW == 16) {

@@ -145,15 +145,17 @@ __global__ void chunk_owner_kernel(ChunkList cl, int32_t *__restrict__ chunk_lon
 }  // namespace
 
 cudaError_t launch_row_softmax(int64_t n_rows, const int32_t *row_ptr, int H, float *S,
-                               const ChunkList &cl, float *ml, float *row_ml, cudaStream_t s) {
+                               const ChunkList &cl_in, float *ml, float *row_ml, cudaStream_t s) {
   // group size: a power of two that H divides when possible, else a full warp
   int GS = 32;
   const bool divides = (32 % H) == 0;
   if (divides) {
     GS = H < 8 ? 8 : H;
   }
-  const int ipb = items_per_block_for(GS, 1);
-  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
+  const Deal dl = deal_items(cl_in, n_rows, GS, 1);
+  const ChunkList &cl = dl.cl;
+  const int ipb = dl.ipb;
+  const int64_t grid = dl.grid;
   if (grid > 0) {
     if (divides)
       softmax_rows_kernel<<<(unsigned)grid, kBlock, 0, s>>>(n_rows, row_ptr, H, GS, S, cl, ipb, ml);

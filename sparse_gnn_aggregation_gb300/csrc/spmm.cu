@@ -41,96 +41,75 @@ __device__ __forceinline__ void accum(float &acc, float &comp, float w, float x)
   }
 }
 
-// Edge weights of U edges p, p + E, ... for every fragment slot.
+// Column indices and edge weights of the U edges p, p + E, ... (those below
+// pe; the others get column 0 and are never used) for every fragment slot.
 // Slots share one weight when there is one head or every slot of the lane
 // lies in the same head (`one`); otherwise each slot loads its head's weight.
 template <int U, int NV>
 __device__ __forceinline__ void load_weights(const int32_t *__restrict__ col_idx,
                                              const float *__restrict__ vals, int H, int es, bool one,
-                                             const int (&head)[NV], int p, int E, int (&c)[U],
+                                             const int (&head)[NV], int p, int E, int pe, int (&c)[U],
                                              float (&w)[U][NV]) {
 #pragma unroll
-  for (int u = 0; u < U; ++u) c[u] = ld_stream_i32(col_idx + p + u * E);
+  for (int u = 0; u < U; ++u) c[u] = p + u * E < pe ? ld_stream_i32(col_idx + p + u * E) : 0;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    if (vals == nullptr) {
+    const int q = p + u * E;
+    if (vals == nullptr || q >= pe) {
 #pragma unroll
       for (int k = 0; k < NV; ++k) w[u][k] = 1.f;
     } else if (H == 1 || one) {
-      const float x = H == 1 ? ld_stream_f32(vals + (int64_t)(p + u * E) * es)
-                             : __ldg(vals + (int64_t)(p + u * E) * es + head[0]);
+      const float x = H == 1 ? ld_stream_f32(vals + (int64_t)q * es) : __ldg(vals + (int64_t)q * es + head[0]);
 #pragma unroll
       for (int k = 0; k < NV; ++k) w[u][k] = x;
     } else {
 #pragma unroll
-      for (int k = 0; k < NV; ++k) w[u][k] = __ldg(vals + (int64_t)(p + u * E) * es + head[k]);
+      for (int k = 0; k < NV; ++k) w[u][k] = __ldg(vals + (int64_t)q * es + head[k]);
     }
   }
 }
 
 // Accumulate edges p = p0, p0 + E, ... < pe into acc (per lane fragments).
-// Full iterations take U edges per edge lane; the next iteration's column
-// indices and weights are loaded while this iteration's rows are in flight,
-// so each iteration waits on one memory round trip, not two.
+// Each round takes U edges per edge lane, predicated at the row's end (a
+// short row is one round with all its loads in flight); the next round's
+// column indices and weights are loaded while this round's rows are in
+// flight, so a round waits on one memory round trip, not two.
 template <typename T, int VW, int NV, int U, bool COMP>
 __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx,
                                              const float *__restrict__ vals, int H, int es, bool one,
                                              const int (&head)[NV], const T *__restrict__ X,
                                              int64_t ldx, int nfrag, const int (&frag)[NV], int E, int p0,
                                              int pe, float (&acc)[NV][VW], float (&comp)[NV][VW]) {
-  int p = p0;
-  if constexpr (U > 1) {
-    if (p + (U - 1) * E < pe) {
-      int c[U];
-      float w[U][NV];
-      load_weights<U, NV>(col_idx, vals, H, es, one, head, p, E, c, w);
-      while (true) {
-        Frag<T, VW> f[U][NV];
+  if (p0 >= pe) return;
+  int c[U];
+  float w[U][NV];
+  load_weights<U, NV>(col_idx, vals, H, es, one, head, p0, E, pe, c, w);
+  for (int p = p0; p < pe; p += U * E) {
+    Frag<T, VW> f[U][NV];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int k = 0; k < NV; ++k)
-            if (frag[k] < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)frag[k] * VW);
-        const int pn = p + U * E;
-        const bool more = pn + (U - 1) * E < pe;
-        int cn[U];
-        float wn[U][NV];
-        if (more) load_weights<U, NV>(col_idx, vals, H, es, one, head, pn, E, cn, wn);
+      for (int k = 0; k < NV; ++k)
+        if (p + u * E < pe && frag[k] < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)frag[k] * VW);
+    const int pn = p + U * E;
+    int cn[U];
+    float wn[U][NV];
+    if (pn < pe) load_weights<U, NV>(col_idx, vals, H, es, one, head, pn, E, pe, cn, wn);
+    // rows of edges past the end were never loaded: skip them (0 * garbage may be NaN)
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u)
+      if (p + u * E < pe)
 #pragma unroll
-          for (int k = 0; k < NV; ++k)
-            if (frag[k] < nfrag)
+        for (int k = 0; k < NV; ++k)
+          if (frag[k] < nfrag)
 #pragma unroll
-              for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[u][k], f[u][k].get(v));
-        p = pn;
-        if (!more) break;
+            for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[u][k], f[u][k].get(v));
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          c[u] = cn[u];
+    for (int u = 0; u < U; ++u) {
+      c[u] = cn[u];
 #pragma unroll
-          for (int k = 0; k < NV; ++k) w[u][k] = wn[u][k];
-        }
-      }
+      for (int k = 0; k < NV; ++k) w[u][k] = wn[u][k];
     }
-  }
-  for (; p < pe; p += E) {
-    const int c = ld_stream_i32(col_idx + p);
-    float w[NV];
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-      w[k] = vals == nullptr ? 1.f
-             : H == 1        ? __ldg(vals + (int64_t)p * es)
-                             : __ldg(vals + (int64_t)p * es + head[one ? 0 : k]);
-    Frag<T, VW> f[NV];
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (frag[k] < nfrag) f[k].load(X + (int64_t)c * ldx + (int64_t)frag[k] * VW);
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (frag[k] < nfrag)
-#pragma unroll
-        for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[k], f[k].get(v));
   }
 }
 
@@ -334,9 +313,11 @@ __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
 template <typename T, int VW>
 cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
                     const float *vals, const T *X, int64_t ldx, T *Y, int64_t ldy,
-                    const ChunkList &cl, float *partial, cudaStream_t s) {
-  const int ipb = items_per_block_for(g.G * g.E, g.G);
-  const int64_t grid = (cl.n_chunks + n_rows + ipb - 1) / ipb;
+                    const ChunkList &cl_in, float *partial, cudaStream_t s) {
+  const Deal dl = deal_items(cl_in, n_rows, g.G * g.E, g.G);
+  const ChunkList &cl = dl.cl;
+  const int ipb = dl.ipb;
+  const int64_t grid = dl.grid;
   if (grid > 0) {
 #define AUTOSAGE_SPMM_K(NVV, CMP)                                                                 \
   spmm_rows_kernel<T, VW, NVV, CMP><<<(unsigned)grid, kBlock, 0, s>>>(                          \
