@@ -140,6 +140,18 @@ template <int VW> __device__ __forceinline__ void store_partial(float *p, const 
 // [chunk_begin[c], min(chunk_begin[c] + split, row end)) of row chunk_row[c]
 // and writes its partial result at slot c. Long row j owns the consecutive
 // chunks [long_ptr[j], long_ptr[j+1]), so a fix-up combines them in order.
+// Runs of a launch: the items are cut into segments (the chunks; then the
+// rows, one segment per degree bucket when the rows are in degree-binned
+// order), and each segment is dealt to its own blocks in runs of run[s]
+// items. Set by deal_items for each launch; n == 0 leaves one uniform run.
+constexpr int kMaxRuns = 34;  // chunks, 32 degree buckets, rows longer than split
+struct RunTable {
+  int n = 0;
+  int64_t item0[kMaxRuns + 1];  // first item of segment s; item0[n] = items
+  int block0[kMaxRuns + 1];     // first block of segment s; block0[n] = grid
+  int run[kMaxRuns];            // items per block in segment s
+};
+
 struct ChunkList {
   const int32_t *chunk_row = nullptr;    // [n_chunks]
   const int32_t *chunk_begin = nullptr;  // [n_chunks]
@@ -149,7 +161,10 @@ struct ChunkList {
   int n_chunks = 0;
   int n_long = 0;
   int split = 0;  // 0: no row is cut
-  int chunk_run = 0;  // chunks per block of a launch (set by deal_items)
+  // degree-binned order: rows of bucket k (k = 0: the longest) start at
+  // position bucket_start[k] of row_order; bucket_start[32] = n_rows
+  int32_t bucket_start[33] = {};
+  RunTable runs;
 };
 
 // One work item: (row, edge begin, edge end, chunk slot or -1 for a whole row).
@@ -186,25 +201,30 @@ __device__ __forceinline__ Item item_at(int64_t idx, int64_t n_rows, const int32
   return it;
 }
 
-// Items of a launch are dealt to blocks: first the chunks of cut rows, in
-// runs of `cl.chunk_run` (a few per lane group: chunks are the longest
-// items), then the rows in runs of `ipb`. Inside a block the lane groups take the block's
-// items one at a time from a shared counter, so a group that drew short rows
-// goes on with the next item instead of idling until the block's longest row
-// ends. Groups of one warp may take different numbers of items; all their
-// shuffles use group or sub-group masks.
+// Items of a launch (the chunks of cut rows, then the rows) are dealt to
+// blocks segment by segment (RunTable): chunks a few per lane group, rows of
+// a degree bucket so many per lane group that a group gets about 1024 edges
+// (at most the plain row run), other rows in plain runs. Inside a block the
+// lane groups take the block's items one at a time from a shared counter, so
+// a group that drew short rows goes on with the next item instead of idling
+// until the block's longest row ends. Groups of one warp may take different
+// numbers of items; all their shuffles use group or sub-group masks.
 struct ItemQueue {
   int64_t base, end;
   int *counter;
   __device__ __forceinline__ ItemQueue(int64_t n_rows, const ChunkList &cl, int ipb, int *shared_counter) {
-    // selects, not branches: the branchy form cost the gather kernels registers
-    const int run = cl.chunk_run > 0 ? cl.chunk_run : ipb;
-    const unsigned chunk_blocks = (static_cast<unsigned>(cl.n_chunks) + run - 1) / run;  // n_chunks < 2^31
-    const bool in_chunks = blockIdx.x < chunk_blocks;
-    base = in_chunks ? (int64_t)blockIdx.x * run : cl.n_chunks + (int64_t)(blockIdx.x - chunk_blocks) * ipb;
-    const int64_t lim = in_chunks ? (int64_t)cl.n_chunks : n_rows + cl.n_chunks;
-    const int64_t stop = base + (in_chunks ? run : ipb);
-    end = stop < lim ? stop : lim;
+    const RunTable &T = cl.runs;
+    if (T.n > 0) {
+      int sg = 0;
+      while (sg + 1 < T.n && (int)blockIdx.x >= T.block0[sg + 1]) ++sg;
+      base = T.item0[sg] + (int64_t)((int)blockIdx.x - T.block0[sg]) * T.run[sg];
+      const int64_t stop = base + T.run[sg];
+      end = stop < T.item0[sg + 1] ? stop : T.item0[sg + 1];
+    } else {
+      base = (int64_t)blockIdx.x * ipb;
+      const int64_t n_items = n_rows + cl.n_chunks;
+      end = base + ipb < n_items ? base + ipb : n_items;
+    }
     counter = shared_counter;
     if (threadIdx.x == 0) *counter = 0;
     __syncthreads();
@@ -227,11 +247,7 @@ inline int items_per_block_for(int GE, int G) {
 }
 
 // The deal of one launch over n_rows rows with lane groups of GE lanes: the
-// chunk list with its chunk run set, the row run, and the grid that covers
-// both (blocks of chunks first). A chunk block gives each lane group about
-// 512 edges (one chunk of 512 or more, four of 128, at most as many chunks
-// as a row block gives it rows): a block of long chunks would otherwise run
-// long after the rest of the grid has finished.
+// chunk list with its run table set, the plain row run, and the grid.
 struct Deal {
   ChunkList cl;
   int ipb;
@@ -240,13 +256,40 @@ struct Deal {
 inline Deal deal_items(const ChunkList &cl, int64_t n_rows, int GE, int G) {
   Deal d{cl, items_per_block_for(GE, G), 0};
   const int groups = (kBlock / 32) * (32 / GE);
+  const int max_per_group = d.ipb / groups;
+  RunTable &T = d.cl.runs;
+  T.n = 0;
+  int64_t item = 0, block = 0;
+  auto add = [&](int64_t count, int run) {
+    if (count <= 0) return;
+    T.item0[T.n] = item;
+    T.block0[T.n] = static_cast<int>(block);
+    T.run[T.n] = run;
+    item += count;
+    block += (count + run - 1) / run;
+    ++T.n;
+  };
+  // chunks: about 512 edges per lane group
   int per_group = cl.split > 0 ? 512 / cl.split : 1;
-  per_group = per_group < 1 ? 1 : (per_group > d.ipb / groups ? d.ipb / groups : per_group);
-  d.cl.chunk_run = groups * per_group;
-  const int64_t chunk_blocks = (cl.n_chunks + d.cl.chunk_run - 1) / d.cl.chunk_run;
-  d.grid = chunk_blocks + (n_rows + d.ipb - 1) / d.ipb;
+  per_group = per_group < 1 ? 1 : (per_group > max_per_group ? max_per_group : per_group);
+  add(cl.n_chunks, groups * per_group);
+  if (cl.row_order && cl.bucket_start[32] == n_rows) {
+    // degree buckets, longest first: bucket k holds degrees below 2^(31 - k)
+    // (the last bucket: rows longer than split, which are inactive items)
+    for (int k = 0; k < 32; ++k) {
+      const int bits = 31 - k;
+      int pg = k == 31 || bits >= 11 ? 1 : 1024 >> bits;
+      if (k == 31) pg = max_per_group;
+      pg = pg < 1 ? 1 : (pg > max_per_group ? max_per_group : pg);
+      add((int64_t)cl.bucket_start[k + 1] - cl.bucket_start[k], groups * pg);
+    }
+  } else {
+    add(n_rows, d.ipb);
+  }
+  T.item0[T.n] = item;
+  T.block0[T.n] = static_cast<int>(block);
+  d.grid = block;
   return d;
 }
-
 
 }  // namespace autosage

@@ -523,7 +523,8 @@ cudaError_t csr_transpose(int64_t n_rows, int64_t n_cols, int64_t nnz, const int
   return err;
 }
 
-cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order, cudaStream_t s) {
+cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order,
+                            int32_t *bucket_start, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
   const int64_t n_tiles = (n_rows + kSortTile - 1) / kSortTile;
   int32_t *keys = nullptr, *keys_out = nullptr, *vals = nullptr, *hist = nullptr, *offs = nullptr;
@@ -543,6 +544,13 @@ cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, i
     radix_scatter_kernel<<<(unsigned)n_tiles, kSortThreads, 0, s>>>(keys, vals, n_rows, 0, n_tiles, offs, keys_out,
                                                                      order);
     err = cudaGetLastError();
+    // where each key starts in the order: the scanned count of tile 0 of its digit
+    for (int k = 0; k < 32 && err == cudaSuccess && bucket_start; ++k)
+      err = cudaMemcpyAsync(bucket_start + k, offs + (int64_t)k * n_tiles, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess && bucket_start) {
+      err = cudaStreamSynchronize(s);
+      bucket_start[32] = static_cast<int32_t>(n_rows);
+    }
   }
   for (int i = 0; i < 5; ++i)
     if (*bufs[i]) cudaFreeAsync(*bufs[i], s);

@@ -110,7 +110,11 @@ cudaError_t launch_attention_backward(const Geom &g, int64_t n_rows, const int32
 cudaError_t launch_invert_perm(int64_t n, const int32_t *perm, int32_t *inv, cudaStream_t s);
 // Degree-binned row order: rows sorted (stably) by degree bucket, longest first,
 // rows longer than `split` last. order: [n_rows]. Temporaries from cudaMallocAsync.
-cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order, cudaStream_t s);
+// bucket_start (host, optional, 33 entries): where rows of key k start in the
+// order (key 0: the longest degree bucket; key 31: empty rows and rows longer
+// than split); bucket_start[32] = n_rows. Synchronises s when given.
+cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order,
+                            int32_t *bucket_start, cudaStream_t s);
 // combined[p] = edge_type[p] * n_cols + col_idx[p]; *err (device) gets 1 for a type out of range.
 cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const int32_t *col_idx,
                                const int32_t *edge_type, int32_t *combined, int *err, cudaStream_t s);

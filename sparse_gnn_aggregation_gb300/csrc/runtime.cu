@@ -435,7 +435,8 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
     st = build_split(P, P->sched.split, s);
     if (st == AUTOSAGE_OK && P->sched.kind == AUTOSAGE_SCHED_BINNED && P->k_rows > 0) {
       CUDA_TRY(P->row_order.alloc(sizeof(int32_t) * (size_t)P->k_rows));
-      CUDA_TRY(build_row_order(P->k_rows, P->k_row_ptr, P->sched.split, P->row_order.as<int32_t>(), s));
+      CUDA_TRY(build_row_order(P->k_rows, P->k_row_ptr, P->sched.split, P->row_order.as<int32_t>(),
+                               P->cl.bucket_start, s));
       P->cl.row_order = P->row_order.as<int32_t>();
     }
   } else if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
