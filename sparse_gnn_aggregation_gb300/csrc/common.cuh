@@ -203,7 +203,7 @@ __device__ __forceinline__ Item item_at(int64_t idx, int64_t n_rows, const int32
 
 // Items of a launch (the chunks of cut rows, then the rows) are dealt to
 // blocks segment by segment (RunTable): chunks a few per lane group, rows of
-// a degree bucket so many per lane group that a group gets about 1024 edges
+// a degree bucket so many per lane group that a group gets about 512 edges
 // (at most the plain row run), other rows in plain runs. Inside a block the
 // lane groups take the block's items one at a time from a shared counter, so
 // a group that drew short rows goes on with the next item instead of idling
@@ -278,7 +278,7 @@ inline Deal deal_items(const ChunkList &cl, int64_t n_rows, int GE, int G) {
     // (the last bucket: rows longer than split, which are inactive items)
     for (int k = 0; k < 32; ++k) {
       const int bits = 31 - k;
-      int pg = k == 31 || bits >= 11 ? 1 : 1024 >> bits;
+      int pg = k == 31 || bits >= 10 ? 1 : 512 >> bits;
       if (k == 31) pg = max_per_group;
       pg = pg < 1 ? 1 : (pg > max_per_group ? max_per_group : pg);
       add((int64_t)cl.bucket_start[k + 1] - cl.bucket_start[k], groups * pg);
