@@ -79,6 +79,9 @@ typedef struct {
   int lanes_f;     /* G: lanes across the feature vector (power of two, 1..32); 0 = auto */
   int lanes_e;     /* E: lanes across edges of one row (power of two, G*E <= 32); 0 = auto */
   int split;       /* SPLIT/BINNED: chunk length in edges; MERGEPATH: items per warp; 0 = auto */
+  int per_edge;    /* SDDMM with one head: 1 = finish each edge's dot product with its own
+                      shuffle reduction; 0 = lane groups of 4 or more lanes reduce batches of
+                      4 or 8 edges with one transpose-reduction. Other ops ignore it. */
 } autosage_schedule;
 
 /* A CSR matrix in device memory. Rows are destinations, col_idx are sources.

@@ -56,7 +56,7 @@ class _Csr(ctypes.Structure):
 
 class _Schedule(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("lanes_f", ctypes.c_int), ("lanes_e", ctypes.c_int),
-                ("split", ctypes.c_int)]
+                ("split", ctypes.c_int), ("per_edge", ctypes.c_int)]
 
 
 def _load():
@@ -213,7 +213,7 @@ class Plan:
         ms = ctypes.c_double()
         _check(_lib.autosage_plan_schedule(self.handle, ctypes.byref(s), ctypes.byref(ms)))
         return {"kind": s.kind, "lanes_f": s.lanes_f, "lanes_e": s.lanes_e, "split": s.split,
-                "probe_ms": ms.value}
+                "per_edge": s.per_edge, "probe_ms": ms.value}
 
     def close(self):
         if self.handle and self.handle.value:
@@ -244,10 +244,10 @@ def autosage_plan(A: CsrMatrix, op: int, F: int, heads: int = 1, dtype=None, fla
 
 
 def autosage_plan_with_schedule(A: CsrMatrix, op: int, F: int, kind: int, lanes_f: int = 0, lanes_e: int = 0,
-                                split: int = 0, heads: int = 1, dtype=None, stream=None) -> Plan:
+                                split: int = 0, heads: int = 1, dtype=None, stream=None, per_edge: int = 0) -> Plan:
     torch = _torch()
     dt = BF16 if dtype == torch.bfloat16 else F32
-    s = _Schedule(kind, lanes_f, lanes_e, split)
+    s = _Schedule(kind, lanes_f, lanes_e, split, int(bool(per_edge)))
     h = ctypes.c_void_p()
     _check(_lib.autosage_plan_with_schedule(A.c, op, int(F), int(heads), dt, ctypes.byref(s), ctypes.byref(h),
                                             _stream(stream)))

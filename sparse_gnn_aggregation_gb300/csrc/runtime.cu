@@ -236,6 +236,7 @@ autosage_status gpu_row_stats(int64_t n_rows, const int32_t *row_ptr, int64_t th
 struct Sched {
   int kind = AUTOSAGE_SCHED_ROWGROUP;
   int G = 0, E = 0, split = 0;
+  int pe = 0;  // SDDMM, one head: per-edge shuffle reductions instead of batched ones
 };
 
 }  // namespace
@@ -515,6 +516,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
     case AUTOSAGE_OP_SDDMM: {
       st = choose_geom(P->dt, 1, P->F, {{a.Q, a.ldq}, {a.K, a.ldk}}, P->sched.G, P->sched.E, true, 16, g);
       if (st != AUTOSAGE_OK) return st;
+      if (P->sched.pe) g.batched = false;
       e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.ldq, a.K, a.ldk, a.alpha, a.S, cl, s);
       break;
     }
@@ -835,7 +837,7 @@ autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &
 }
 
 bool same_sched(const Sched &a, const Sched &b) {
-  return a.kind == b.kind && a.G == b.G && a.E == b.E && a.split == b.split;
+  return a.kind == b.kind && a.G == b.G && a.E == b.E && a.split == b.split && a.pe == b.pe;
 }
 
 struct Candidate {
@@ -872,6 +874,8 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
   const int G0 = std::min(32, pow2ceil(nfrag));
   Gs.push_back(G0);
   if (G0 > 1 && P->op != AUTOSAGE_OP_SOFTMAX) Gs.push_back(G0 / 2);
+  // SDDMM with per-edge reductions ran fastest with four fragments a lane
+  if (P->op == AUTOSAGE_OP_SDDMM && G0 >= 16) Gs.push_back(G0 / 4);
   const int64_t maxd = st.ints[2];
   for (int G : Gs) {
     if (P->op == AUTOSAGE_OP_SOFTMAX && G != G0) continue;
@@ -900,14 +904,27 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
       }
     }
   }
+  // single-head SDDMM: every candidate with 4 or more feature lanes also with
+  // per-edge reductions (measured: faster on uniform rows at F >= 64, slower
+  // on skewed rows and at small F; the estimate does not tell them apart)
+  if (P->op == AUTOSAGE_OP_SDDMM) {
+    const size_t n = out.size();
+    for (size_t i = 0; i < n; ++i) {
+      if (out[i].sc.G < 4) continue;
+      Candidate c = out[i];
+      c.sc.pe = 1;
+      out.push_back(c);
+    }
+  }
   std::stable_sort(out.begin(), out.end(), [](const Candidate &a, const Candidate &b) { return a.est < b.est; });
   return out;
 }
 
 // Neighbours of a schedule for the probes' local refinement: half or twice
 // the edge lanes, half or twice the feature lanes, a quarter or four times
-// the chunk length (merge path: the items per warp), and the other chunked
-// family (split <-> binned) with the same lanes and chunk length. Automatic
+// the chunk length (merge path: the items per warp), the other chunked
+// family (split <-> binned) with the same lanes and chunk length, and for
+// SDDMM the other reduction form (per edge <-> batched). Automatic
 // lanes (0) are first resolved the way the kernels resolve them.
 std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *P, const RowStats &st,
                                   const Sched &b) {
@@ -927,6 +944,7 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
   auto add = [&](Sched x) {
     Geom g{};
     if (!cand_geom(P, x.G, x.E, g)) return;
+    if (P->op != AUTOSAGE_OP_SDDMM || x.G < 4) x.pe = 0;
     if (softmax && x.E != 1) return;
     if (x.kind == AUTOSAGE_SCHED_MERGEPATH) {
       if (x.G * x.E != 32 || (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)) return;
@@ -945,16 +963,17 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
   for (int e2 : {E / 2, E * 2}) {
     if (e2 < 1 || e2 > 32) continue;
     // merge path keeps whole warps: the feature lanes follow the edge lanes
-    add(Sched{b.kind, b.kind == AUTOSAGE_SCHED_MERGEPATH ? 32 / e2 : G, e2, b.split});
+    add(Sched{b.kind, b.kind == AUTOSAGE_SCHED_MERGEPATH ? 32 / e2 : G, e2, b.split, b.pe});
   }
   if (b.kind != AUTOSAGE_SCHED_MERGEPATH && !softmax)
     for (int g2 : {G / 2, G * 2})
-      if (g2 >= 1) add(Sched{b.kind, g2, E, b.split});
+      if (g2 >= 1) add(Sched{b.kind, g2, E, b.split, b.pe});
   if (b.kind != AUTOSAGE_SCHED_ROWGROUP)
-    for (int s2 : {b.split / 4, b.split * 4}) add(Sched{b.kind, G, E, s2});
-  if (b.kind == AUTOSAGE_SCHED_SPLIT) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split});
-  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_SPLIT, G, E, b.split});
-  if (b.kind == AUTOSAGE_SCHED_ROWGROUP && maxd > 128) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, 128});
+    for (int s2 : {b.split / 4, b.split * 4}) add(Sched{b.kind, G, E, s2, b.pe});
+  if (b.kind == AUTOSAGE_SCHED_SPLIT) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe});
+  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_SPLIT, G, E, b.split, b.pe});
+  if (b.kind == AUTOSAGE_SCHED_ROWGROUP && maxd > 128) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, 128, b.pe});
+  if (P->op == AUTOSAGE_OP_SDDMM) add(Sched{b.kind, G, E, b.split, 1 - b.pe});
   return out;
 }
 
@@ -1045,7 +1064,7 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
   autosage_plan_s *P = nullptr;
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
-  P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split};
+  P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split, sched->per_edge ? 1 : 0};
   if ((P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED) && P->sched.split == 0)
     P->sched.split = 1024;
   if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH && P->sched.split == 0) P->sched.split = 512;
@@ -1150,8 +1169,9 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
     for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH, AUTOSAGE_SCHED_BINNED}) {
       std::vector<int> seen_g;
       for (const Candidate &c : cands) {
-        if (c.sc.kind != kind || std::find(seen_g.begin(), seen_g.end(), c.sc.G) != seen_g.end()) continue;
-        seen_g.push_back(c.sc.G);
+        const int gk = c.sc.G * 2 + c.sc.pe;
+        if (c.sc.kind != kind || std::find(seen_g.begin(), seen_g.end(), gk) != seen_g.end()) continue;
+        seen_g.push_back(gk);
         top.push_back(c);
       }
     }
@@ -1182,6 +1202,9 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
       }
     }
     int ok_count = 0;
+    // fastest schedule of each reduction form (SDDMM: batched, per edge)
+    double form_ms[2] = {-1, -1};
+    Sched form_best[2];
     auto probe_one = [&](const Candidate &c) {
       P->sched = c.sc;
       if (build_workspace(P, s) != AUTOSAGE_OK) {
@@ -1215,28 +1238,37 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
         }
       }
       ++ok_count;
-      log_line("plan key=%s probe %s G=%d E=%d split=%d est_ms=%.4f probe_ms=%.4f", key.c_str(),
-               sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, c.est * 1e3, ms);
+      log_line("plan key=%s probe %s G=%d E=%d split=%d pe=%d est_ms=%.4f probe_ms=%.4f", key.c_str(),
+               sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, c.sc.pe, c.est * 1e3, ms);
       if (best_ms < 0 || ms < best_ms) {
         best_ms = ms;
         best = c.sc;
         best_est = c.est;
+      }
+      const int f = c.sc.pe ? 1 : 0;
+      if (form_ms[f] < 0 || ms < form_ms[f]) {
+        form_ms[f] = ms;
+        form_best[f] = c.sc;
       }
     };
     for (const Candidate &c : top) probe_one(c);
     // local refinement: the estimate ranks edge lanes and chunk lengths
     // poorly, so the neighbours of the fastest schedule are probed too, and
     // again around each new fastest one (at most four rounds)
+    // (separately for each reduction form: their best lane counts differ)
     std::vector<Sched> tried;
     for (const Candidate &c : top) tried.push_back(c.sc);
-    for (int round = 0; round < 4 && best_ms >= 0; ++round) {
-      const Sched centre = best;
-      for (const Candidate &c : neighbours(dev, P, rs, centre)) {
-        if (std::any_of(tried.begin(), tried.end(), [&](const Sched &t) { return same_sched(t, c.sc); })) continue;
-        tried.push_back(c.sc);
-        probe_one(c);
+    for (int f = 0; f < 2; ++f) {
+      for (int round = 0; round < 4 && form_ms[f] >= 0; ++round) {
+        const Sched centre = form_best[f];
+        for (const Candidate &c : neighbours(dev, P, rs, centre)) {
+          if ((c.sc.pe ? 1 : 0) != f) continue;
+          if (std::any_of(tried.begin(), tried.end(), [&](const Sched &t) { return same_sched(t, c.sc); })) continue;
+          tried.push_back(c.sc);
+          probe_one(c);
+        }
+        if (same_sched(form_best[f], centre)) break;
       }
-      if (same_sched(best, centre)) break;
     }
     cudaGetLastError();  // a failed candidate must not poison later calls
     if (ok_count == 0) {
@@ -1276,9 +1308,9 @@ autosage_status autosage_plan_destroy(autosage_plan_t plan) {
 autosage_status autosage_plan_describe(autosage_plan_t P, char *buf, size_t len) {
   if (!P || !buf || len == 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad describe arguments");
   snprintf(buf, len, "op=%d sched=%s G=%d E=%d split=%d chunks=%d long_rows=%d mp_warps=%" PRId64
-           " probe_ms=%.4f est_ms=%.4f cache=%d",
+           " probe_ms=%.4f est_ms=%.4f cache=%d per_edge=%d",
            (int)P->op, sched_name(P->sched.kind), P->sched.G, P->sched.E, P->sched.split, P->cl.n_chunks,
-           P->cl.n_long, P->mp_warps, P->probe_ms, P->est_ms, P->from_cache ? 1 : 0);
+           P->cl.n_long, P->mp_warps, P->probe_ms, P->est_ms, P->from_cache ? 1 : 0, P->sched.pe);
   return AUTOSAGE_OK;
 }
 
@@ -1289,6 +1321,7 @@ autosage_status autosage_plan_schedule(autosage_plan_t P, autosage_schedule *sch
     sched->lanes_f = P->sched.G;
     sched->lanes_e = P->sched.E;
     sched->split = P->sched.split;
+    sched->per_edge = P->sched.pe;
   }
   if (probe_ms) *probe_ms = P->probe_ms;
   return AUTOSAGE_OK;
@@ -1641,8 +1674,9 @@ autosage_status autosage_cache_save(const char *path) {
     std::lock_guard<std::mutex> lk(g_cache_mu);
     fprintf(f, "%s\n", kCacheHeader);
     for (const auto &kv : g_cache)
-      fprintf(f, "%s\t%s %d %d %d %.6f\n", kv.first.c_str(), sched_name(kv.second.sched.kind),
-              kv.second.sched.G, kv.second.sched.E, kv.second.sched.split, kv.second.probe_ms);
+      fprintf(f, "%s\t%s %d %d %d %.6f%s\n", kv.first.c_str(), sched_name(kv.second.sched.kind),
+              kv.second.sched.G, kv.second.sched.E, kv.second.sched.split, kv.second.probe_ms,
+              kv.second.sched.pe ? " edge" : "");
   }
   const bool ok = fflush(f) == 0;
   fclose(f);
@@ -1674,10 +1708,15 @@ autosage_status autosage_cache_load(const char *path) {
       ++bad;
       continue;
     }
+    // optional marker: per-edge SDDMM reductions
     std::string rest;
     if (vs >> rest) {
-      ++bad;
-      continue;
+      std::string more;
+      if (rest != "edge" || (vs >> more)) {
+        ++bad;
+        continue;
+      }
+      e.sched.pe = 1;
     }
     if (kind == "rowgroup") e.sched.kind = AUTOSAGE_SCHED_ROWGROUP;
     else if (kind == "split") e.sched.kind = AUTOSAGE_SCHED_SPLIT;

@@ -30,6 +30,20 @@ def test_round_trip(tmp_path, sga):
     assert sga.autosage_cache_size() == 0
 
 
+def test_per_edge_marker_round_trip(tmp_path, sga):
+    # an SDDMM entry with per-edge reductions carries the optional `edge` marker
+    sga.autosage_cache_clear()
+    line = "NVIDIA_GB300|sm152|op2|dt0|F64|H1|n10|m10|nnz20|fp00000000000000ab\trowgroup 16 1 0 0.250000 edge\n"
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + GOOD + line)
+    sga.autosage_cache_load(str(p))
+    assert sga.autosage_cache_size() == 2
+    q = tmp_path / "d.txt"
+    sga.autosage_cache_save(str(q))
+    assert sorted(q.read_text().splitlines()[1:]) == sorted([GOOD.strip(), line.strip()])
+    sga.autosage_cache_clear()
+
+
 def test_wrong_header_rejected(tmp_path, sga):
     sga.autosage_cache_clear()
     p = tmp_path / "c.txt"
@@ -48,6 +62,7 @@ def test_wrong_header_rejected(tmp_path, sga):
     "key\trowgroup 3 1 0 0.1\n",               # lanes not a power of two
     "key\tsplit 16 4 0 0.1\n",                 # split schedule without a chunk length
     "key\trowgroup 16 4 0 0.1 extra\n",        # trailing field
+    "key\trowgroup 16 4 0 0.1 edge edge\n",    # marker twice
     "\tsplit 16 2 512 0.1\n",                  # empty key
 ])
 def test_corrupt_lines_are_skipped(tmp_path, sga, bad):

@@ -151,6 +151,29 @@ def test_sddmm_width_sweep_skewed(skew, F, name, spec):
     assert_close(to_np(S), oracle.sddmm(g.row_ptr, g.col_idx, Q, K, 0.5)[:, 0], TOL_F32, f"sddmm F={F} {name}")
 
 
+PER_EDGE = [
+    ("rowgroup-g4", dict(kind=sga.SCHED_ROWGROUP, lanes_f=4, lanes_e=1, per_edge=1)),
+    ("rowgroup-g8-e2", dict(kind=sga.SCHED_ROWGROUP, lanes_f=8, lanes_e=2, per_edge=1)),
+    ("binned-g16", dict(kind=sga.SCHED_BINNED, lanes_f=16, split=32, per_edge=1)),
+    ("split-g4-e4", dict(kind=sga.SCHED_SPLIT, lanes_f=4, lanes_e=4, split=16, per_edge=1)),
+]
+
+
+@pytest.mark.parametrize("F", [16, 20, 64, 100, 256])
+@pytest.mark.parametrize("name,spec", PER_EDGE, ids=[s[0] for s in PER_EDGE])
+def test_sddmm_per_edge_reduction(skew, F, name, spec):
+    # single-head SDDMM with one shuffle reduction per edge instead of batched
+    # transpose-reductions (a planner variant); same results within tolerance
+    g = skew
+    A = mat(g)
+    Q = synth.normal(g.n_rows, F, 12, synth.STREAM_Q)
+    K = synth.normal(g.n_cols, F, 12, synth.STREAM_K)
+    plan = make_plan(A, sga.OP_SDDMM, F, spec)
+    assert plan.schedule()["per_edge"] == 1 and "per_edge=1" in plan.describe()
+    S = sga.autosage_sddmm(A, dev(Q), dev(K), 0.25, plan=plan)
+    assert_close(to_np(S), oracle.sddmm(g.row_ptr, g.col_idx, Q, K, 0.25)[:, 0], TOL_F32, f"sddmm F={F} {name}")
+
+
 def test_sddmm_bf16(skew):
     g = skew
     A = mat(g)

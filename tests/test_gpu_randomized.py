@@ -51,8 +51,9 @@ def plan_for(rng, A, op, F, heads, dtype, allow_mergepath):
     split = int(rng.choice([1, 3, 16, 64]))
     if kind == sga.SCHED_ROWGROUP:
         split = 0
+    per_edge = int(op == sga.OP_SDDMM and rng.random() < 0.5)
     return sga.autosage_plan_with_schedule(A, op, F, kind, lanes_e=0 if kind == sga.SCHED_MERGEPATH else lanes_e,
-                                           split=split, heads=heads, dtype=dtype)
+                                           split=split, heads=heads, dtype=dtype, per_edge=per_edge)
 
 
 @pytest.mark.parametrize("seed", range(24))
