@@ -608,7 +608,43 @@ def cpu_baseline(graphs, budget_s=15.0, steps=1):
     return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"a seeded uniform {100 * frac:.2f}% of the rows of each graph for every operation of "
                       f"the step ({b / 1e9:.2f} GB algorithmic, {t:.1f} s)",
-            "per_op": per_op}
+            "per_op": per_op, "single_core_ms": single_core_ms()}
+
+
+def single_core_ms():
+    """The oracle on one thread for the two small workloads the survey times
+    that way: the tiny Erdos-Renyi graph (SpMM, SDDMM, attention at F = 32)
+    and the benchmark page's shape (384 nodes, degree 18, edge-softmax
+    aggregation with given scores at F = 64). Median of 3 runs, ms."""
+    import oracle
+
+    def med(fn):
+        ts = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return round(1e3 * float(np.median(ts)), 3)
+
+    oracle.set_threads(1)
+    try:
+        g = synth.tiny_er(0)
+        X, Q, K, V = (synth.normal(g.n_rows, 32, 0, st) for st in
+                      (synth.STREAM_X, synth.STREAM_Q, synth.STREAM_K, synth.STREAM_V))
+        p = synth.attention_benchmark_shape(0)
+        S = synth.normal(p.nnz, 1, 0, synth.STREAM_Q)
+        PV = synth.normal(p.n_rows, 64, 0, synth.STREAM_V)
+        out = {
+            "tiny_er/spmm/F32": med(lambda: oracle.spmm(g.row_ptr, g.col_idx, g.vals, X)),
+            "tiny_er/sddmm/F32": med(lambda: oracle.sddmm(g.row_ptr, g.col_idx, Q, K, 1.0)),
+            "tiny_er/attention/H1D32": med(lambda: oracle.csr_attention(g.row_ptr, g.col_idx, Q, K, V, 1,
+                                                                        1.0 / np.sqrt(32))),
+            "page_shape/edge_softmax_aggregate/F64": med(lambda: oracle.edge_softmax_aggregate(
+                p.row_ptr, p.col_idx, S, PV)),
+        }
+    finally:
+        oracle.set_threads(oracle.threads())
+    return out
 
 
 def run_reference(args):

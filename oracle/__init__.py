@@ -66,6 +66,8 @@ def _bind(path: str):
     lib.oracle_csr_attention_backward.restype = None
     lib.oracle_spmm_typed.argtypes = [_i64, _i64, _ptr, _ptr, _ptr, _ptr, _ptr, _i64, _i64, _ptr]
     lib.oracle_spmm_typed.restype = None
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads.restype = None
     lib.oracle_fingerprint.argtypes = [_i64, _ptr, _ptr]
     lib.oracle_fingerprint.restype = ctypes.c_uint64
     for name in ("oracle_spmm", "oracle_sddmm", "oracle_row_softmax", "oracle_csr_attention",
@@ -309,6 +311,11 @@ def fingerprint(row_ptr, col_idx) -> int:
     lib = _load()
     row_ptr, col_idx = _i32(row_ptr), _i32(col_idx)
     return int(lib.oracle_fingerprint(row_ptr.shape[0] - 1, _p(row_ptr), _p(col_idx)))
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's row-parallel loops (timing only; results do not depend on it)."""
+    _load().oracle_set_threads(int(n))
 
 
 def threads() -> int:

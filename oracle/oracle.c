@@ -26,6 +26,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ROW(k) (rows ? rows[(k)] : (int64_t)(k))
 
@@ -311,4 +314,14 @@ void oracle_spmm_typed(int64_t n_rows, int64_t n_cols, const int32_t *row_ptr, c
       for (int64_t f = 0; f < F; ++f) y[f] += w * (double)z[f];
     }
   }
+}
+
+/* Threads of the row-parallel loops (timing only: every row is computed by
+ * one thread in a fixed order, so results do not depend on it). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
 }
