@@ -79,16 +79,15 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
         q[k].zero();
     }
   }
-  float m[NG], l[NG], acc[NV][VW];
+  float m[NG], l[NG];
+  Acc<VW> acc[NV];
 #pragma unroll
   for (int j = 0; j < NG; ++j) {
     m[j] = -INFINITY;
     l[j] = 0.f;
   }
 #pragma unroll
-  for (int k = 0; k < NV; ++k)
-#pragma unroll
-    for (int v = 0; v < VW; ++v) acc[k][v] = 0.f;
+  for (int k = 0; k < NV; ++k) acc[k].zero();
   constexpr int U = NV * VW <= 8 ? 4 : 2;
   int c[U];
 #pragma unroll
@@ -130,14 +129,8 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
 #pragma unroll
         for (int j = 0; j < NG; ++j) s[u][j] = 0.f;
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-          if (valid[k]) {
-            float d = 0.f;
-#pragma unroll
-            for (int v = 0; v < VW; ++v) d = fmaf(q[k].get(v), fk[u][k].get(v), d);
-            s[u][ONE ? 0 : k] += d;
-          }
-        }
+        for (int k = 0; k < NV; ++k)
+          if (valid[k]) s[u][ONE ? 0 : k] += frag_dot(q[k], fk[u][k]);
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
           for (int off = 1; off < R; off <<= 1) s[u][j] += __shfl_xor_sync(L.sub_mask, s[u][j], off);
@@ -163,9 +156,7 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
         l[j] *= corr;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-          if (ONE || k == j)
-#pragma unroll
-            for (int v = 0; v < VW; ++v) acc[k][v] *= corr;
+          if (ONE || k == j) acc[k].scale(corr);
         m[j] = mx;
       }
 #pragma unroll
@@ -180,9 +171,7 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
       if (valid[k])
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (live[u])
-#pragma unroll
-            for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[u][ONE ? 0 : k], fv[u][k].get(v), acc[k][v]);
+          if (live[u]) acc[k].fma(w[u][ONE ? 0 : k], fv[u][k]);
   }
   // merge the E edge-lane states (fixed xor order)
   for (int off = G; off < L.GE; off <<= 1) {
@@ -199,8 +188,8 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
         if (!(ONE || k == j)) continue;
 #pragma unroll
         for (int v = 0; v < VW; ++v) {
-          const float ao = __shfl_xor_sync(L.group_mask, acc[k][v], off);
-          acc[k][v] = acc[k][v] * a + ao * b;
+          const float ao = __shfl_xor_sync(L.group_mask, acc[k].get(v), off);
+          acc[k].set(v, acc[k].get(v) * a + ao * b);
         }
       }
       m[j] = mx;
@@ -216,7 +205,7 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
       const float inv = lk > 0.f ? 1.f / lk : 0.f;
       float r[VW];
 #pragma unroll
-      for (int v = 0; v < VW; ++v) r[v] = acc[k][v] * inv;
+      for (int v = 0; v < VW; ++v) r[v] = acc[k].get(v) * inv;
       store_frag<T, VW>(o + (int64_t)frag[k] * VW, r);
     }
   } else {
@@ -224,7 +213,10 @@ __global__ void __launch_bounds__(kBlock, attn_min_blocks<T, VW, NV>()) attentio
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       if (!valid[k]) continue;
-      store_partial<VW>(pa + (int64_t)frag[k] * VW, acc[k]);
+      float r[VW];
+#pragma unroll
+      for (int v = 0; v < VW; ++v) r[v] = acc[k].get(v);
+      store_partial<VW>(pa + (int64_t)frag[k] * VW, r);
       if (frag[k] % cph == 0) {
         const int h = H > 1 ? frag[k] / cph : 0;
         float *pm = part_ml + ((int64_t)it.chunk * H + h) * 2;

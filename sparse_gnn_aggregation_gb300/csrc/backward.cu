@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
         go[k].zero();
       }
     }
-    float m[NG], l[NG], sw[NG], a[NV][VW], b[NV][VW];
+    float m[NG], l[NG], sw[NG];
+    Acc<VW> a[NV], b[NV];
 #pragma unroll
     for (int j = 0; j < NG; ++j) {
       m[j] = -INFINITY;
@@ -113,12 +114,10 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
       sw[j] = 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-      for (int v = 0; v < VW; ++v) {
-        a[k][v] = 0.f;
-        b[k][v] = 0.f;
-      }
+    for (int k = 0; k < NV; ++k) {
+      a[k].zero();
+      b[k].zero();
+    }
     int c[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -158,14 +157,8 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
           if (live[u] && valid[k]) {
-            float d1 = 0.f, d2 = 0.f;
-#pragma unroll
-            for (int v = 0; v < VW; ++v) {
-              d1 = fmaf(q[k].get(v), fk[u][k].get(v), d1);
-              d2 = fmaf(go[k].get(v), fv[u][k].get(v), d2);
-            }
-            s[u][ONE ? 0 : k] += d1;
-            dw[u][ONE ? 0 : k] += d2;
+            s[u][ONE ? 0 : k] += frag_dot(q[k], fk[u][k]);
+            dw[u][ONE ? 0 : k] += frag_dot(go[k], fv[u][k]);
           }
         }
 #pragma unroll
@@ -203,12 +196,10 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
           sw[j] *= corr;
 #pragma unroll
           for (int k = 0; k < NV; ++k)
-            if (ONE || k == j)
-#pragma unroll
-              for (int v = 0; v < VW; ++v) {
-                a[k][v] *= corr;
-                b[k][v] *= corr;
-              }
+            if (ONE || k == j) {
+              a[k].scale(corr);
+              b[k].scale(corr);
+            }
           m[j] = mx;
         }
 #pragma unroll
@@ -226,13 +217,8 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
           for (int u = 0; u < U; ++u)
             if (live[u]) {
               const float e1 = ew[u][ONE ? 0 : k];
-              const float e2 = e1 * dw[u][ONE ? 0 : k];
-#pragma unroll
-              for (int v = 0; v < VW; ++v) {
-                const float kv = fk[u][k].get(v);
-                a[k][v] = fmaf(e2, kv, a[k][v]);
-                b[k][v] = fmaf(e1, kv, b[k][v]);
-              }
+              a[k].fma(e1 * dw[u][ONE ? 0 : k], fk[u][k]);
+              b[k].fma(e1, fk[u][k]);
             }
     }
     // merge the E edge-lane states (fixed xor order); every lane ends with the group's state
@@ -252,10 +238,10 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
           if (!(ONE || k == j)) continue;
 #pragma unroll
           for (int v = 0; v < VW; ++v) {
-            const float ao = __shfl_xor_sync(L.group_mask, a[k][v], off);
-            const float bo = __shfl_xor_sync(L.group_mask, b[k][v], off);
-            a[k][v] = a[k][v] * fa + ao * fb;
-            b[k][v] = b[k][v] * fa + bo * fb;
+            const float ao = __shfl_xor_sync(L.group_mask, a[k].get(v), off);
+            const float bo = __shfl_xor_sync(L.group_mask, b[k].get(v), off);
+            a[k].set(v, a[k].get(v) * fa + ao * fb);
+            b[k].set(v, b[k].get(v) * fa + bo * fb);
           }
         }
         m[j] = mx;
@@ -269,8 +255,14 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
         if (!valid[k]) continue;
-        store_partial<VW>(pa + (int64_t)frag[k] * VW, a[k]);
-        store_partial<VW>(pa + width + (int64_t)frag[k] * VW, b[k]);
+        float ra[VW], rb[VW];
+#pragma unroll
+        for (int v = 0; v < VW; ++v) {
+          ra[v] = a[k].get(v);
+          rb[v] = b[k].get(v);
+        }
+        store_partial<VW>(pa + (int64_t)frag[k] * VW, ra);
+        store_partial<VW>(pa + width + (int64_t)frag[k] * VW, rb);
       }
       if (writer) {
 #pragma unroll
@@ -299,7 +291,7 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
         const int j = ONE ? 0 : k;
         float r[VW];
 #pragma unroll
-        for (int v = 0; v < VW; ++v) r[v] = scale * (a[k][v] - dd[j] * b[k][v]) * il[j];
+        for (int v = 0; v < VW; ++v) r[v] = scale * (a[k].get(v) - dd[j] * b[k].get(v)) * il[j];
         store_frag<T, VW>(o + (int64_t)frag[k] * VW, r);
       }
     }

@@ -49,7 +49,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // A fragment of VW consecutive elements of type T kept in its raw (packed)
-// form; get(i) widens element i to fp32.
+// form; get(i) widens element i to fp32, get2(i) elements 2i and 2i + 1 as a
+// pair for the packed fp32x2 arithmetic of sm_100 and later (VW even).
 template <typename T, int VW> struct Frag;
 
 template <> struct Frag<float, 4> {
@@ -57,12 +58,14 @@ template <> struct Frag<float, 4> {
   __device__ __forceinline__ void load(const float *p) { r = __ldg(reinterpret_cast<const float4 *>(p)); }
   __device__ __forceinline__ void zero() { r = make_float4(0.f, 0.f, 0.f, 0.f); }
   __device__ __forceinline__ float get(int i) const { return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w; }
+  __device__ __forceinline__ float2 get2(int i) const { return i == 0 ? make_float2(r.x, r.y) : make_float2(r.z, r.w); }
 };
 template <> struct Frag<float, 2> {
   float2 r;
   __device__ __forceinline__ void load(const float *p) { r = __ldg(reinterpret_cast<const float2 *>(p)); }
   __device__ __forceinline__ void zero() { r = make_float2(0.f, 0.f); }
   __device__ __forceinline__ float get(int i) const { return i == 0 ? r.x : r.y; }
+  __device__ __forceinline__ float2 get2(int) const { return r; }
 };
 template <> struct Frag<float, 1> {
   float r;
@@ -78,6 +81,10 @@ template <> struct Frag<__nv_bfloat16, 8> {
     const uint32_t w = i < 2 ? r.x : i < 4 ? r.y : i < 6 ? r.z : r.w;
     return (i & 1) ? bf16hi(w) : bf16lo(w);
   }
+  __device__ __forceinline__ float2 get2(int i) const {
+    const uint32_t w = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
+    return make_float2(bf16lo(w), bf16hi(w));
+  }
 };
 template <> struct Frag<__nv_bfloat16, 4> {
   uint2 r;
@@ -87,12 +94,17 @@ template <> struct Frag<__nv_bfloat16, 4> {
     const uint32_t w = i < 2 ? r.x : r.y;
     return (i & 1) ? bf16hi(w) : bf16lo(w);
   }
+  __device__ __forceinline__ float2 get2(int i) const {
+    const uint32_t w = i == 0 ? r.x : r.y;
+    return make_float2(bf16lo(w), bf16hi(w));
+  }
 };
 template <> struct Frag<__nv_bfloat16, 2> {
   uint32_t r;
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const unsigned int *>(p)); }
   __device__ __forceinline__ void zero() { r = 0u; }
   __device__ __forceinline__ float get(int i) const { return (i & 1) ? bf16hi(r) : bf16lo(r); }
+  __device__ __forceinline__ float2 get2(int) const { return make_float2(bf16lo(r), bf16hi(r)); }
 };
 template <> struct Frag<__nv_bfloat16, 1> {
   uint32_t r;
@@ -102,6 +114,53 @@ template <> struct Frag<__nv_bfloat16, 1> {
   __device__ __forceinline__ void zero() { r = 0u; }
   __device__ __forceinline__ float get(int) const { return __uint_as_float(r << 16); }
 };
+
+// A running fp32 sum over one fragment slot: VW values kept as pairs, so
+// that the accumulation runs on the packed fp32x2 FMA of sm_100 and later
+// (one instruction for two elements; each element is still one fp32 FMA,
+// rounded to nearest). VW = 1 keeps its one value in .x.
+template <int VW>
+struct Acc {
+  static constexpr int P = (VW + 1) / 2;
+  float2 p[P];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < P; ++i) p[i] = make_float2(0.f, 0.f);
+  }
+  __device__ __forceinline__ void scale(float c) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) p[i] = __fmul2_rn(p[i], make_float2(c, c));
+  }
+  template <typename F>
+  __device__ __forceinline__ void fma(float w, const F &f) {
+    if constexpr (VW >= 2) {
+      const float2 ww = make_float2(w, w);
+#pragma unroll
+      for (int i = 0; i < P; ++i) p[i] = __ffma2_rn(ww, f.get2(i), p[i]);
+    } else {
+      p[0].x = fmaf(w, f.get(0), p[0].x);
+    }
+  }
+  __device__ __forceinline__ float get(int v) const { return (v & 1) ? p[v >> 1].y : p[v >> 1].x; }
+  __device__ __forceinline__ void set(int v, float x) {
+    if (v & 1) p[v >> 1].y = x;
+    else p[v >> 1].x = x;
+  }
+};
+
+// <a, b> over one fragment pair: even and odd elements in two packed
+// fp32x2 chains, added at the end.
+template <typename T, int VW>
+__device__ __forceinline__ float frag_dot(const Frag<T, VW> &a, const Frag<T, VW> &b) {
+  if constexpr (VW >= 2) {
+    float2 d = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < VW / 2; ++i) d = __ffma2_rn(a.get2(i), b.get2(i), d);
+    return d.x + d.y;
+  } else {
+    return a.get(0) * b.get(0);
+  }
+}
 
 // Store VW fp32 values as type T (bf16: round to nearest even), streaming.
 template <typename T, int VW> __device__ __forceinline__ void store_frag(T *p, const float (&o)[VW]);
