@@ -361,7 +361,7 @@ def run_ours(args):
         tot_nnzF += g.nnz * width
     step_ms, value = aggregate_ranks(tot_ms, tot_bytes, world, dev)
 
-    # rows beyond the step (SURVEY "next"): CSR-attention backward on the same graph
+    # rows beyond the step: the CSR-attention backward on the same graph
     next_rows = {}
     if not args.no_next and (not args.only or "backward" in args.only.split(",")):
         g = graphs["rmat"]

@@ -25,7 +25,7 @@ def lib_path():
     return build.build()
 
 
-def test_header_declares_the_north_star_api():
+def test_header_declares_the_core_api():
     syms = declared_symbols()
     for name in ("autosage_spmm", "autosage_sddmm", "autosage_csr_attention", "autosage_plan",
                  "autosage_plan_destroy", "autosage_cache_load", "autosage_cache_save",
