@@ -119,6 +119,48 @@ def test_rmat20_attention_bf16(rmat20, fused):
     assert_close(got, ref, TOL_BF16, f"attention fused={fused} [{plan.describe()}]")
 
 
+def test_rmat20_attention_backward_bf16(rmat20):
+    # the backward in the benchmark's configuration (bf16, H = 8, D = 64,
+    # default backward plan). dQ of a row depends on that row's edges only,
+    # so the oracle runs on the sub-graph of sampled rows (columns renumbered
+    # to the ones they touch); dK and dV are checked at full size through two
+    # identities of the chain rule: sum_j dV_j = sum of dO over non-empty rows
+    # (each row's weights sum to 1) and sum_j dK_j = 0 (each row's score
+    # gradients sum to 0).
+    g = rmat20
+    A = mat(g)
+    H, D = 8, 64
+    W = H * D
+    Qb, Q32 = bf16_tensor(synth.normal(g.n_rows, W, 11, synth.STREAM_Q))
+    Kb, K32 = bf16_tensor(synth.normal(g.n_cols, W, 11, synth.STREAM_K))
+    Vb, V32 = bf16_tensor(synth.normal(g.n_cols, W, 11, synth.STREAM_V))
+    Gb, G32 = bf16_tensor(synth.normal(g.n_rows, W, 11, synth.STREAM_G))
+    plan = sga.autosage_plan(A, sga.OP_ATTN_BACKWARD, D, heads=H, dtype=torch.bfloat16)
+    dQ, dK, dV = sga.autosage_csr_attention_backward(A, Qb, Kb, Vb, Gb, H, 0.125, plan=plan)
+    torch.cuda.synchronize()
+
+    rows = sample_rows(g, n=200, top=5)
+    deg = (g.row_ptr[rows + 1] - g.row_ptr[rows]).astype(np.int64)
+    sub_ptr = np.zeros(rows.size + 1, np.int32)
+    np.cumsum(deg, out=sub_ptr[1:])
+    cols = np.concatenate([g.col_idx[g.row_ptr[r]:g.row_ptr[r + 1]] for r in rows])
+    used, sub_cols = np.unique(cols, return_inverse=True)
+    rQ, _, _ = oracle.csr_attention_backward(sub_ptr, sub_cols.astype(np.int32), Q32[rows], K32[used],
+                                             V32[used], G32[rows], H, 0.125)
+    got = dQ[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert_close(got, rQ, TOL_BF16, f"backward dQ [{plan.describe()}]")
+
+    nonempty = np.diff(g.row_ptr) > 0
+    want_dv = G32.astype(np.float64)[nonempty].sum(0)
+    dv_sum = dV.double().sum(0).cpu().numpy()
+    dk_sum = dK.double().sum(0).cpu().numpy()
+    # bf16 outputs carry at most 2^-9 relative rounding each
+    tol_dv = 4e-3 * dV.double().abs().sum(0).cpu().numpy() + 1e-3
+    tol_dk = 4e-3 * dK.double().abs().sum(0).cpu().numpy() + 1e-3
+    assert np.all(np.abs(dv_sum - want_dv) <= tol_dv), "sum of dV != sum of dO over non-empty rows"
+    assert np.all(np.abs(dk_sum) <= tol_dk), "sum of dK != 0"
+
+
 @pytest.fixture(scope="module")
 def products():
     return synth.products_like(seed=0)

@@ -1,12 +1,14 @@
 """Pins for the oracle's CSR-attention backward (no GPU).
 
-The backward is checked against two things other than itself: central finite
-differences of the oracle's own forward (the definition of a derivative), and
-torch autograd through a dense masked attention in float64 on the CPU."""
+The backward is checked against things other than itself: central finite
+differences of the oracle's own forward (the definition of a derivative),
+torch autograd through a dense masked attention in float64 on the CPU, and
+two column-sum identities that follow from the softmax."""
 import numpy as np
 import pytest
 
 import oracle
+import synth
 
 
 def small_graph(seed=0, n=9, m=7, p=0.5):
@@ -80,3 +82,17 @@ def test_backward_matches_torch_autograd_dense():
     np.testing.assert_allclose(dQ, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dK, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dV, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_backward_column_sum_identities():
+    # each row's softmax weights sum to 1 and its score gradients to 0, so
+    # sum_j dV_j = sum of dO over non-empty rows and sum_j dK_j = 0 (per head)
+    g = synth.rmat_skew(10, seed=4)
+    H, D = 2, 8
+    Q, dO = (synth.normal(g.n_rows, H * D, 5, st) for st in (synth.STREAM_Q, synth.STREAM_G))
+    K, V = (synth.normal(g.n_cols, H * D, 5, st) for st in (synth.STREAM_K, synth.STREAM_V))
+    dQ, dK, dV = oracle.csr_attention_backward(g.row_ptr, g.col_idx, Q, K, V, dO, H, 0.3)
+    nonempty = np.diff(g.row_ptr) > 0
+    assert (~nonempty).any()  # the identity must hold with empty rows present
+    np.testing.assert_allclose(dV.sum(0), dO.astype(np.float64)[nonempty].sum(0), rtol=1e-12, atol=1e-10)
+    np.testing.assert_allclose(dK.sum(0), 0.0, atol=1e-10)
