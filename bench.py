@@ -180,10 +180,18 @@ class ClockSampler:
         try:
             self.fh = open(self.out, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: wait for its first sample so
+        # that the samples cover the timed region that follows
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 3.0 and self.proc.poll() is None:
+            if os.path.getsize(self.out) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
