@@ -96,3 +96,46 @@ def test_backward_column_sum_identities():
     assert (~nonempty).any()  # the identity must hold with empty rows present
     np.testing.assert_allclose(dV.sum(0), dO.astype(np.float64)[nonempty].sum(0), rtol=1e-12, atol=1e-10)
     np.testing.assert_allclose(dK.sum(0), 0.0, atol=1e-10)
+
+
+BACKWARD_MUTATIONS = [
+    # (description, original text, planted mistake)
+    ("dS drops the row sum D", "const double ds = w[p - b] * (dw[p - b] - Di);",
+     "const double ds = w[p - b] * dw[p - b];"),
+    ("dK gathers K instead of Q", "dK[j * F + h * D + d] += scale * ds * (double)q[d];",
+     "dK[j * F + h * D + d] += scale * ds * (double)k[d];"),
+    ("dQ without the score scale", "dQ[i * F + h * D + d] += scale * ds * (double)k[d];",
+     "dQ[i * F + h * D + d] += ds * (double)k[d];"),
+    ("dV weighted by dW instead of w", "dV[j * F + h * D + d] += w[p - b] * (double)go[d];",
+     "dV[j * F + h * D + d] += dw[p - b] * (double)go[d];"),
+]
+
+
+def _backward_pins_fail() -> bool:
+    pins = [lambda: test_backward_matches_finite_differences(1, 3),
+            lambda: test_backward_matches_finite_differences(2, 2),
+            test_backward_column_sum_identities]
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("desc,orig,bad", BACKWARD_MUTATIONS, ids=[m[0] for m in BACKWARD_MUTATIONS])
+def test_planted_backward_mistake_is_caught(tmp_path, desc, orig, bad):
+    import os
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    assert orig in src, f"mutation anchor missing: {orig!r}"
+    c = tmp_path / "oracle_bad.c"
+    c.write_text(src.replace(orig, bad))
+    so = tmp_path / "liboracle_bad.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-std=c11", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    with oracle.use_library(str(so)):
+        assert _backward_pins_fail(), f"planted mistake not caught: {desc}"
