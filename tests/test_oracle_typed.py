@@ -2,6 +2,7 @@
 sum over relations of the pinned single-relation SpMM on each relation's
 edges, and dense brute force sum_r A_r Z_r."""
 import numpy as np
+import pytest
 
 import oracle
 
@@ -31,3 +32,31 @@ def test_typed_spmm_is_sum_of_relations():
     # one relation reduces to plain SpMM exactly
     np.testing.assert_array_equal(oracle.spmm_typed(row_ptr, col_idx, np.zeros_like(etype), vals, Z[:1]),
                                   oracle.spmm(row_ptr, col_idx, vals, Z[0]))
+
+
+TYPED_MUTATIONS = [
+    ("relation ignored", "const float *z = Z + ((int64_t)edge_type[p] * n_cols + col_idx[p]) * ldz;",
+     "const float *z = Z + ((int64_t)col_idx[p]) * ldz;"),
+    ("edge value dropped", "      const double w = vals ? (double)vals[p] : 1.0;\n      const float *z = Z",
+     "      const double w = 1.0;\n      const float *z = Z"),
+]
+
+
+
+@pytest.mark.parametrize("desc,orig,bad", TYPED_MUTATIONS, ids=[m[0] for m in TYPED_MUTATIONS])
+def test_planted_typed_mistake_is_caught(tmp_path, desc, orig, bad):
+    import os
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    assert orig in src, f"mutation anchor missing: {orig!r}"
+    c = tmp_path / "oracle_bad.c"
+    c.write_text(src.replace(orig, bad))
+    so = tmp_path / "liboracle_bad.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-std=c11", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    with oracle.use_library(str(so)):
+        with pytest.raises(AssertionError):
+            test_typed_spmm_is_sum_of_relations()
