@@ -69,3 +69,38 @@ def test_host_side_argument_checks_need_no_gpu(lib_path):
     h = ctypes.c_void_p()
     assert lib.autosage_plan_with_schedule(ctypes.byref(c), 0, 4, 1, 0, ctypes.byref(sched), ctypes.byref(h),
                                            None) == sga.ERR_INVALID_ARG
+
+
+def test_header_is_plain_c_and_a_c_program_links(lib_path, tmp_path):
+    # the boundary is usable from C: the header compiles as C11 (no C++ or
+    # torch types), and a C program links against the library and calls the
+    # entry points that need no GPU
+    import shutil
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "autosage.h"
+int main(void) {
+  autosage_schedule s;
+  memset(&s, 0, sizeof s);
+  s.kind = AUTOSAGE_SCHED_BINNED;
+  s.per_edge = 1;
+  const char *v = autosage_version();
+  const char *e = autosage_status_string(AUTOSAGE_ERR_INVALID_CSR);
+  /* a NULL CSR is an argument error, reported before any launch */
+  autosage_status st = autosage_spmm(NULL, NULL, 0, NULL, 0, 4, AUTOSAGE_F32, 0, NULL, NULL);
+  printf("%s|%s|%d|%d\n", v, e, (int)st, (int)(st == AUTOSAGE_ERR_INVALID_ARG));
+  return st == AUTOSAGE_ERR_INVALID_ARG ? 0 : 1;
+}
+""")
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(lib_path)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-lautosage", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    version, err, _, ok = out.stdout.strip().split("|")
+    assert version.startswith("autosage") and "CSR" in err and ok == "1"
