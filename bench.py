@@ -43,7 +43,7 @@ import synth  # noqa: E402
 FS = [4, 8, 16, 32, 64, 128, 256]
 HEADS, HEAD_DIM = 8, 64
 METRIC = "SpMM/SDDMM/CSR-attn achieved HBM GB/s (% of ~8 TB/s) and nnz·F/s on 1 GB300"
-WORKLOAD = "R-MAT scale 20 (ef 16, a,b,c,d=.57,.19,.19,.05) + uniform-degree control; fp32 F sweep 4..256 SpMM+SDDMM; SpMM A^T F=64; bf16 CSR attention H=8 D=64 fused+unfused"
+WORKLOAD = "R-MAT s20 ef16 + uniform control: SpMM/SDDMM F4-256 f32, SpMM^T F64, bf16 attn H8 D64"
 
 
 def dist_env():
@@ -137,6 +137,15 @@ def attn_backward_bytes(n, m, nnz, H, D, s):
     return rows + 2 * spmm_t
 
 
+def workload_config(graphs, world):
+    """The `config` object of both arms' lines (identical keys and values)."""
+    rm, un = graphs["rmat"], graphs["uniform"]
+    return {"workload": WORKLOAD, "nodes": rm.n_rows, "nnz_rmat": rm.nnz, "nnz_uniform": un.nnz,
+            "max_degree_rmat": int(rm.degrees().max()),
+            "l2": "GPU arm: a 2x-L2 buffer is overwritten before every operation, outside the timed spans",
+            "parallelism": f"replicas x{world}"}
+
+
 def op_list(graphs, only=None):
     """(key, kind, graph, F) in execution order; graphs alternate so the other
     graph's data sits between two uses of one CSR. `only` keeps keys containing it."""
@@ -162,6 +171,113 @@ def op_bytes(kind, g, F):
         return sddmm_bytes(n, nnz, F, 4), 2 * nnz * F
     fused = kind == "attn_fused"
     return attn_bytes(n, nnz, HEADS, HEAD_DIM, 2, fused), 2 * nnz * HEADS * HEAD_DIM
+
+
+# ---------------------------------------------------------------- the two largest configs
+
+def large_config_rows(dev, flush, stream, steps, warmup, oracle_frac=0.05):
+    """Throughput on the products-like and Reddit-like graphs, measured like
+    the step (L2 flushed before every launch, CUDA events on the launching
+    stream, algorithmic bytes), with the oracle timed beside each operation
+    on a seeded uniform sample of the rows (fraction ``oracle_frac``):
+      products-like (2,449,029 nodes, 123.7M edges, mean aggregation):
+        SpMM at F = 32 and 100, SpMM with A^T at F = 32 and 100, and the A^T
+        build (once per plan) on its own;
+      Reddit-like (232,965 nodes, 114.6M edges, 50 communities):
+        SpMM at F = 128 and 602, SDDMM at F = 128."""
+    import ctypes
+
+    import torch
+
+    import oracle
+    import sparse_gnn_aggregation_gb300 as sga
+
+    oracle.build()
+    peak, _ = measured_peak()
+    out = {}
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.fill_(1.0)
+            fn()
+        evs = []
+        for _ in range(steps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    def oracle_rate(kind, g, F, X, gt=None):
+        rng = np.random.default_rng(54321)
+        src = gt if kind == "spmm_t" else g
+        k = max(1, int(round(src.n_rows * oracle_frac)))
+        rows = np.sort(rng.choice(src.n_rows, size=k, replace=False)).astype(np.int64)
+        enn = int((src.row_ptr[rows + 1] - src.row_ptr[rows]).sum())
+        t0 = time.perf_counter()
+        if kind == "sddmm":
+            oracle.sddmm(src.row_ptr, src.col_idx, X, X, 1.0, rows=rows)
+            b = sddmm_bytes(rows.size, enn, F, 4)
+        else:
+            oracle.spmm(src.row_ptr, src.col_idx, src.vals, X, rows=rows)
+            b = spmm_bytes(rows.size, enn, F, 4)
+        dt = time.perf_counter() - t0
+        return {"GBps": round(b / dt / 1e9, 3), "rows_sampled": int(rows.size), "s": round(dt, 3),
+                "cores": oracle.threads()}
+
+    flags = sga.PLAN_PROBE | sga.PLAN_VERIFY
+    for gname, gen, ops in (("products", synth.products_like, [("spmm", 32), ("spmm", 100), ("spmm_t", 32),
+                                                               ("spmm_t", 100)]),
+                            ("reddit", synth.reddit_like, [("spmm", 128), ("spmm", 602), ("sddmm", 128)])):
+        g = gen(seed=0)
+        A = sga.CsrMatrix.from_numpy(g.row_ptr, g.col_idx, g.vals, g.n_cols)
+        gt = None
+        if any(k == "spmm_t" for k, _ in ops):
+            rpt, cit, vt = oracle.transpose(g.row_ptr, g.col_idx, g.vals, g.n_cols)
+            gt = synth.Csr(g.n_cols, g.n_rows, rpt, cit, vt)
+            t_rp = torch.empty(g.n_cols + 1, dtype=torch.int32, device=dev)
+            t_ci = torch.empty(g.nnz, dtype=torch.int32, device=dev)
+            t_v = torch.empty(g.nnz, dtype=torch.float32, device=dev)
+            lib = sga.library()
+            ms = timed(lambda: lib.autosage_csr_transpose(A.c, ctypes.c_void_p(t_rp.data_ptr()),
+                                                          ctypes.c_void_p(t_ci.data_ptr()),
+                                                          ctypes.c_void_p(t_v.data_ptr()),
+                                                          ctypes.c_void_p(stream.cuda_stream)))
+            out[f"transpose_build/{gname}"] = {"ms": round(ms, 4), "note": "CSR of A^T (stable radix sort), "
+                                               "built once per SpMM^T plan; not part of the SpMM^T rows"}
+            del t_rp, t_ci, t_v
+        for kind, F in ops:
+            key = f"{kind}/{gname}/F{F}"
+            if kind == "sddmm":
+                Q = torch.randn(g.n_rows, F, device=dev)
+                K = torch.randn(g.n_cols, F, device=dev)
+                S = torch.empty(g.nnz, device=dev)
+                plan = sga.autosage_plan(A, sga.OP_SDDMM, F, flags=flags)
+                ms = timed(lambda: sga.autosage_sddmm(A, Q, K, 1.0, S, plan=plan))
+                b = sddmm_bytes(g.n_rows, g.nnz, F, 4)
+                del Q, K, S
+            else:
+                tr = kind == "spmm_t"
+                X = torch.randn(g.n_rows if tr else g.n_cols, F, device=dev)
+                Y = torch.empty(g.n_cols if tr else g.n_rows, F, device=dev)
+                plan = sga.autosage_plan(A, sga.OP_SPMM_T if tr else sga.OP_SPMM, F, flags=flags)
+                ms = timed(lambda: sga.autosage_spmm(A, X, Y, transpose=tr, plan=plan))
+                b = spmm_bytes(g.n_rows, g.nnz, F, 4)
+                del X, Y
+            Xh = np.random.default_rng(2).standard_normal((g.n_rows, F), dtype=np.float32)
+            out[key] = {"ms": round(ms, 4), "GBps": round(b / ms / 1e6, 1),
+                        "frac_of_hbm_peak": round(b / ms / 1e6 / peak, 4),
+                        "nnzF_per_s": g.nnz * F / (ms * 1e-3), "bytes": int(b), "dtype": "f32",
+                        "plan": plan.describe(), "oracle": oracle_rate(kind, g, F, Xh, gt)}
+            del plan
+        del A
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- clocks
@@ -429,6 +545,11 @@ def run_ours(args):
             "bytes": int(b), "dtype": "f32", "plan": tplan.describe()}
         del et, Z, Yt, tplan
 
+    # the products-like and Reddit-like configs: throughput rows beside the step
+    configs = {}
+    if not args.no_configs and (not args.only or "configs" in args.only.split(",")):
+        configs = large_config_rows(dev, flush, stream, args.steps, args.warmup)
+
     # dominant operation: the largest share of the step
     # (one main kernel per launch: the unfused pipeline is three kernels, so it is not a candidate)
     dom_key = max((k for k in per_op if not k.startswith("attn_unfused")), key=lambda k: per_op[k]["ms"])
@@ -515,10 +636,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32 (F sweep, SpMM^T); bf16 in / f32 softmax+acc (attention)",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "nodes": graphs["rmat"].n_rows, "nnz_rmat": graphs["rmat"].nnz,
-                   "nnz_uniform": graphs["uniform"].nnz, "max_degree_rmat": int(graphs["rmat"].degrees().max()),
-                   "l2": "flushed before every operation (2x L2 buffer overwritten, outside the timed spans)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(graphs, world),
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "nnzF_per_s": tot_nnzF * world / (step_ms * 1e-3),
         "edges_per_s": sum(graphs[g].nnz for _, _, g, _ in ops) * world / (step_ms * 1e-3),
@@ -530,6 +648,7 @@ def run_ours(args):
         "plan_seconds": round(plan_s, 2),
         "per_op": per_op,
         "next": next_rows,
+        "configs": configs,
         "source_hash": source_hash(),
     }
     if e2e is not None:
@@ -620,10 +739,11 @@ def cpu_baseline(graphs, budget_s=15.0, steps=1):
 
 
 def single_core_ms():
-    """The oracle on one thread for the two small workloads the survey times
-    that way: the tiny Erdos-Renyi graph (SpMM, SDDMM, attention at F = 32)
-    and the benchmark page's shape (384 nodes, degree 18, edge-softmax
-    aggregation with given scores at F = 64). Median of 3 runs, ms."""
+    """The oracle on one thread for the two small workloads: the tiny
+    Erdos-Renyi graph (4,096 nodes, degree 16; SpMM, SDDMM, attention at
+    F = 32) and the fused attention-aggregation benchmark shape (384 nodes,
+    degree 18, edge-softmax aggregation with given scores at F = 64).
+    Median of 3 runs, ms."""
     import oracle
 
     def med(fn):
@@ -670,7 +790,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-            "config": {"workload": WORKLOAD},
+            "config": workload_config(graphs, world),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "kind": "oracle", "cores": vals[-1]["cores"],
                              "sample": vals[-1]["sample"]},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -687,6 +807,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows measured beyond the step")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the products-like and Reddit-like throughput rows")
     ap.add_argument("--only", default=None, help="run only operations whose key contains one of these comma-separated texts "
                          "(backward, typed: the rows measured beyond the step)")
     ap.add_argument("--scale", type=int, default=20, help="R-MAT scale (20 is the benchmark workload)")

@@ -193,7 +193,12 @@ autosage_status autosage_edge_softmax_aggregate(const autosage_csr *A, const flo
  *    before any launch; no cudaMalloc / cudaFree or allocating routine is called.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
- *    capture.
+ *    capture. The address is kept for the life of the process: after
+ *    cudaDeviceReset (or in another primary context of that device) it is stale,
+ *    so do not call this entry point again after resetting the device.
+ *  - The CSR descriptor gets the same host-side checks as autosage_csr_attention
+ *    (sizes, NULL pointers, 4-byte alignment); the GPU structural validation of
+ *    AUTOSAGE_CHECK=1 is not run here, because it allocates.
  *  - Every call on a device shares the one array and leaves its scores there.
  *    Calls whose work overlaps on the GPU (other streams, other threads) race on
  *    it: serialise them. Nothing in the array needs to start at zero.
@@ -223,6 +228,26 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
                                             int heads, autosage_dtype dt,
                                             const autosage_schedule *sched,
                                             autosage_plan_t *out, void *stream);
+
+/* A plan is bound to the structure of the A it was built for: its workspace (chunk lists,
+ * row order, merge-path partitions, A^T and the edge permutation) is derived from row_ptr
+ * and col_idx. Every op called with a plan therefore requires A->row_ptr and A->col_idx to
+ * be the very arrays given at plan time (same pointers, contents unchanged) and returns
+ * AUTOSAGE_ERR_PLAN_MISMATCH before any launch otherwise; with the environment variable
+ * AUTOSAGE_CHECK=1 it also recomputes the structure fingerprint (synchronising) and
+ * refuses arrays that were overwritten with another graph. The edge values are NOT part
+ * of the binding: every call reads A->vals as passed (for SpMM with A^T they are gathered
+ * into A^T's edge order on the stream at each call), so new values per layer or step need
+ * no new plan. A typed plan is bound to row_ptr, col_idx and edge_type.
+ * A plan's workspace is shared by its calls: calls of one plan that overlap on the GPU
+ * (several streams or threads) race on it; serialise them or use one plan per stream. */
+
+/* Rebind a plan to structure arrays that moved (a copy of the same graph in new device
+ * memory). Computes the fingerprint of A's structure on the GPU (SYNCHRONISES `stream`)
+ * and accepts A only if its sizes and fingerprint equal those of the plan's graph;
+ * otherwise returns AUTOSAGE_ERR_PLAN_MISMATCH and leaves the plan unchanged. Typed plans
+ * return AUTOSAGE_ERR_UNSUPPORTED (their combined index is built from the edge types). */
+autosage_status autosage_plan_rebind(autosage_plan_t plan, const autosage_csr *A, void *stream);
 
 /* Free a plan and its workspace (synchronises the device). NULL is allowed. */
 autosage_status autosage_plan_destroy(autosage_plan_t plan);

@@ -39,7 +39,7 @@ EXPORTS = [
     "autosage_row_stats", "autosage_fingerprint", "autosage_validate_csr", "autosage_csr_transpose",
     "autosage_status_string", "autosage_last_error", "autosage_version",
     "autosage_csr_attention_unfused_noalloc", "autosage_csr_attention_backward",
-    "autosage_plan_typed", "autosage_spmm_typed",
+    "autosage_plan_typed", "autosage_spmm_typed", "autosage_plan_rebind",
 ]
 
 
@@ -79,6 +79,7 @@ def _load():
         "autosage_plan": [CSR, I, I64, I, I, U, ctypes.POINTER(P), P],
         "autosage_plan_with_schedule": [CSR, I, I64, I, I, ctypes.POINTER(_Schedule), ctypes.POINTER(P), P],
         "autosage_plan_destroy": [P],
+        "autosage_plan_rebind": [P, CSR, P],
         "autosage_plan_describe": [P, ctypes.c_char_p, ctypes.c_size_t],
         "autosage_plan_schedule": [P, ctypes.POINTER(_Schedule), ctypes.POINTER(ctypes.c_double)],
         "autosage_cache_load": [ctypes.c_char_p],
@@ -154,6 +155,28 @@ def _ld(t) -> int:
     return int(t.stride(0))
 
 
+def _head_width(T, heads: int):
+    """(W, D) of a [n, heads * D] or [n, heads, D] attention tensor; rejects heads that do not divide W."""
+    heads = int(heads)
+    if heads < 1:
+        raise ValueError("heads must be >= 1")
+    W = int(T.shape[-1]) if T.dim() == 2 else int(T.shape[-1] * T.shape[-2])
+    if W % heads:
+        raise ValueError(f"row width {W} is not a multiple of heads = {heads}")
+    return W, W // heads
+
+
+def _same_layout(ref, rows: int, what: str, *tensors):
+    """Every tensor: contiguous, ref's dtype and device, ``rows`` rows of ref's row width."""
+    for name, t in tensors:
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: {name} must be contiguous")
+        if t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError(f"{what}: {name} must have the dtype and device of the first input")
+        if int(t.shape[0]) != rows or tuple(t.shape[1:]) != tuple(ref.shape[1:]):
+            raise ValueError(f"{what}: {name} has shape {tuple(t.shape)}, expected {(rows,) + tuple(ref.shape[1:])}")
+
+
 # ---------------------------------------------------------------- CSR handle
 
 @dataclasses.dataclass
@@ -215,6 +238,12 @@ class Plan:
         return {"kind": s.kind, "lanes_f": s.lanes_f, "lanes_e": s.lanes_e, "split": s.split,
                 "per_edge": s.per_edge, "probe_ms": ms.value}
 
+    def rebind(self, A: "CsrMatrix", stream=None):
+        """Bind the plan to a copy of its graph's structure in other device memory
+        (checked by fingerprint on the GPU; raises ERR_PLAN_MISMATCH for another graph)."""
+        _check(_lib.autosage_plan_rebind(self.handle, A.c, _stream(stream)))
+        return self
+
     def close(self):
         if self.handle and self.handle.value:
             _lib.autosage_plan_destroy(self.handle)
@@ -252,6 +281,12 @@ def autosage_plan_with_schedule(A: CsrMatrix, op: int, F: int, kind: int, lanes_
     _check(_lib.autosage_plan_with_schedule(A.c, op, int(F), int(heads), dt, ctypes.byref(s), ctypes.byref(h),
                                             _stream(stream)))
     return Plan(h.value, op)
+
+
+def autosage_plan_rebind(plan: Plan, A: CsrMatrix, stream=None) -> Plan:
+    """Bind ``plan`` to A's structure arrays when they moved (same graph in other
+    device memory). Raises AutosageError(ERR_PLAN_MISMATCH) for another graph."""
+    return plan.rebind(A, stream)
 
 
 # ---------------------------------------------------------------- ops
@@ -292,13 +327,11 @@ def autosage_csr_attention(A: CsrMatrix, Q, K, V, heads: int, scale: float, fuse
                            plan: Plan | None = None, stream=None):
     """CSR attention; Q, K, V, out are [n, heads * D] (= [n, heads, D] contiguous)."""
     torch = _torch()
-    W = int(Q.shape[-1]) if Q.dim() == 2 else int(Q.shape[-1] * Q.shape[-2])
-    D = W // heads
+    _, D = _head_width(Q, heads)
     if out is None:
         out = torch.empty_like(Q)
-    for t in (Q, K, V, out):
-        if not t.is_contiguous():
-            raise ValueError("attention tensors must be contiguous")
+    _same_layout(Q, A.n_rows, "attention", ("Q", Q), ("out", out))
+    _same_layout(Q, A.n_cols, "attention", ("K", K), ("V", V))
     _check(_lib.autosage_csr_attention(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), D, _dt(Q), float(scale),
                                        _ptr(out), int(bool(fused)), _plan_handle(plan), _stream(stream)))
     return out
@@ -338,14 +371,13 @@ def autosage_csr_attention_backward(A: CsrMatrix, Q, K, V, dO, heads: int, scale
     built for OP_ATTN_BACKWARD with F = D; without one the call builds a
     temporary plan (allocating and synchronising)."""
     torch = _torch()
-    W = int(Q.shape[-1]) if Q.dim() == 2 else int(Q.shape[-1] * Q.shape[-2])
+    _, D = _head_width(Q, heads)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
-    for t in (Q, K, V, dO, dQ, dK, dV):
-        if not t.is_contiguous() or t.dtype != Q.dtype:
-            raise ValueError("backward tensors must be contiguous and share one dtype")
-    _check(_lib.autosage_csr_attention_backward(A.c, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), int(heads), W // heads,
+    _same_layout(Q, A.n_rows, "attention backward", ("Q", Q), ("dO", dO), ("dQ", dQ))
+    _same_layout(Q, A.n_cols, "attention backward", ("K", K), ("V", V), ("dK", dK), ("dV", dV))
+    _check(_lib.autosage_csr_attention_backward(A.c, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), int(heads), D,
                                                 _dt(Q), float(scale), _ptr(dQ), _ptr(dK), _ptr(dV),
                                                 _plan_handle(plan), _stream(stream)))
     return dQ, dK, dV
@@ -363,11 +395,10 @@ def autosage_csr_attention_unfused_noalloc(A: CsrMatrix, Q, K, V, heads: int, sc
     may not exceed NOALLOC_MAX_SCORES. Calls that overlap on the GPU share
     that array and must be serialised by the caller.
     """
-    W = int(Q.shape[-1]) if Q.dim() == 2 else int(Q.shape[-1] * Q.shape[-2])
-    for t in (Q, K, V, out):
-        if not t.is_contiguous():
-            raise ValueError("attention tensors must be contiguous")
-    _check(_lib.autosage_csr_attention_unfused_noalloc(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), W // heads,
+    _, D = _head_width(Q, heads)
+    _same_layout(Q, A.n_rows, "attention", ("Q", Q), ("out", out))
+    _same_layout(Q, A.n_cols, "attention", ("K", K), ("V", V))
+    _check(_lib.autosage_csr_attention_unfused_noalloc(A.c, _ptr(Q), _ptr(K), _ptr(V), int(heads), D,
                                                        _dt(Q), float(scale), _ptr(out), _stream(stream)))
     return out
 
@@ -376,10 +407,14 @@ def autosage_edge_softmax_aggregate(A: CsrMatrix, scores, V, heads: int = 1, out
                                     stream=None):
     """Softmax of given fp32 scores [nnz, heads] per row, then weighted sum of V rows."""
     torch = _torch()
-    W = int(V.shape[-1]) if V.dim() == 2 else int(V.shape[-1] * V.shape[-2])
+    _, D = _head_width(V, heads)
     if out is None:
         out = torch.empty((A.n_rows,) + tuple(V.shape[1:]), dtype=V.dtype, device=V.device)
-    _check(_lib.autosage_edge_softmax_aggregate(A.c, _ptr(scores), _ptr(V), int(heads), W // heads, _dt(V),
+    _same_layout(V, A.n_cols, "edge softmax aggregation", ("V", V))
+    _same_layout(V, A.n_rows, "edge softmax aggregation", ("out", out))
+    if scores.dtype != torch.float32 or not scores.is_contiguous() or scores.numel() != A.nnz * int(heads):
+        raise ValueError("scores must be a contiguous float32 tensor of nnz * heads elements")
+    _check(_lib.autosage_edge_softmax_aggregate(A.c, _ptr(scores), _ptr(V), int(heads), D, _dt(V),
                                                 _ptr(out), _plan_handle(plan), _stream(stream)))
     return out
 

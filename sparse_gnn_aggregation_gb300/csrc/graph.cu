@@ -315,6 +315,15 @@ __global__ void transpose_gather_kernel(int64_t nnz, const int32_t *__restrict__
 // Sort key of a row for the degree-binned order: 31 - bit_length(degree), so
 // an ascending stable sort puts the longest rows first; rows cut into chunks
 // (degree > split) get 31 and go last (their row items do no work).
+// out[k] = vals[perm[k]]: edge values carried into another edge order
+// (grid-stride; perm is read in order, vals gathered).
+__global__ void gather_vals_kernel(int64_t nnz, const int32_t *__restrict__ perm, const float *__restrict__ vals,
+                                   float *__restrict__ out) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < nnz; k += stride)
+    __stcs(out + k, __ldg(vals + __ldcs(perm + k)));
+}
+
 __global__ void degree_key_kernel(int64_t n_rows, const int32_t *__restrict__ row_ptr, int split,
                                   int32_t *__restrict__ keys, int32_t *__restrict__ vals) {
   const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -556,6 +565,12 @@ cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, i
     if (*bufs[i]) cudaFreeAsync(*bufs[i], s);
   if (scan_tmp) cudaFreeAsync(scan_tmp, s);
   return err;
+}
+
+cudaError_t launch_gather_vals(int64_t nnz, const int32_t *perm, const float *vals, float *out, cudaStream_t s) {
+  if (nnz <= 0) return cudaSuccess;
+  gather_vals_kernel<<<grid_for(nnz, 256, 152 * 32), 256, 0, s>>>(nnz, perm, vals, out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const int32_t *col_idx,

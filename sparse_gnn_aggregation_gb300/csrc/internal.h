@@ -61,12 +61,14 @@ cudaError_t launch_attention(const Geom &g, int64_t n_rows, const int32_t *row_p
 
 // Merge-path SpMM: warp w covers diagonals [w*items, (w+1)*items) of the
 // (rows + edges) merge path; part: [n_warps + 1] int2 (row, edge) starts.
-// carry_val: [n_warps * F] fp32, carry_row: [n_warps] int32.
+// carry_val: [n_warps * F] fp32 (the row left unfinished at a warp's end),
+// carry_row: [n_warps] int32, head_val: [n_warps * F] fp32 (the last segment
+// of a row that earlier warps began, added and rounded by the fix-up).
 cudaError_t launch_spmm_mergepath(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                                   const int32_t *col_idx, const float *vals, const void *X,
                                   int64_t ldx, void *Y, int64_t ldy, const int2 *part,
                                   int64_t n_warps, float *carry_val, int32_t *carry_row,
-                                  cudaStream_t s);
+                                  float *head_val, cudaStream_t s);
 cudaError_t launch_mergepath_partition(int64_t n_rows, int64_t nnz, const int32_t *row_ptr,
                                        int64_t items, int64_t n_warps, int2 *part, cudaStream_t s);
 
@@ -115,6 +117,8 @@ cudaError_t launch_invert_perm(int64_t n, const int32_t *perm, int32_t *inv, cud
 // than split); bucket_start[32] = n_rows. Synchronises s when given.
 cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order,
                             int32_t *bucket_start, cudaStream_t s);
+// out[k] = vals[perm[k]] for k < nnz (edge values carried into A^T's edge order).
+cudaError_t launch_gather_vals(int64_t nnz, const int32_t *perm, const float *vals, float *out, cudaStream_t s);
 // combined[p] = edge_type[p] * n_cols + col_idx[p]; *err (device) gets 1 for a type out of range.
 cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const int32_t *col_idx,
                                const int32_t *edge_type, int32_t *combined, int *err, cudaStream_t s);

@@ -14,6 +14,8 @@
 #include "internal.h"
 
 namespace autosage {
+autosage_status check_attention_args(const autosage_csr *A, const void *Q, const void *K, const void *V, int heads,
+                                     int64_t D, autosage_dtype dt, const void *out);
 autosage_status attention_unfused_with_scores(const autosage_csr *A, const void *Q, const void *K,
                                               const void *V, int heads, int64_t D, autosage_dtype dt,
                                               float scale, void *out, float *scores, cudaStream_t s);
@@ -55,14 +57,15 @@ extern "C" autosage_status autosage_csr_attention_unfused_noalloc(const autosage
                                                                   const void *K, const void *V, int heads,
                                                                   int64_t D, autosage_dtype dt, float scale,
                                                                   void *out, void *stream) {
-  if (!A || heads < 1 || A->nnz < 0)
-    return autosage::report(AUTOSAGE_ERR_INVALID_ARG, "A is NULL, heads < 1 or nnz < 0");
+  // every argument is checked on the host before the device is touched
+  autosage_status st = autosage::check_attention_args(A, Q, K, V, heads, D, dt, out);
+  if (st != AUTOSAGE_OK) return st;
   if ((uint64_t)A->nnz * (uint64_t)heads > (uint64_t)AUTOSAGE_NOALLOC_MAX_SCORES)
     return autosage::report(AUTOSAGE_ERR_UNSUPPORTED,
                             "nnz * heads exceeds the fixed score scratch (AUTOSAGE_NOALLOC_MAX_SCORES = 4194304 "
                             "fp32 elements); use autosage_csr_attention instead");
   float *scores = nullptr;
-  autosage_status st = scratch_address(&scores);
+  st = scratch_address(&scores);
   if (st != AUTOSAGE_OK) return st;
   // every score the softmax and the SpMM read is written by the SDDMM first,
   // so nothing in the scratch has to start at zero

@@ -61,7 +61,10 @@ bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 // ---------------------------------------------------------------- validation
 
-autosage_status check_csr(const autosage_csr *A, bool need_cols) {
+// Host-side checks of a CSR descriptor (sizes, NULL pointers, alignment);
+// with AUTOSAGE_CHECK=1 and gpu_check, also the full structural validation
+// on the GPU (synchronising; it allocates a stream-ordered flag).
+autosage_status check_csr(const autosage_csr *A, bool gpu_check) {
   if (!A) return fail(AUTOSAGE_ERR_INVALID_ARG, "A is NULL");
   if (A->n_rows < 0 || A->n_cols < 0 || A->nnz < 0)
     return fail(AUTOSAGE_ERR_INVALID_ARG, "negative CSR size");
@@ -73,8 +76,7 @@ autosage_status check_csr(const autosage_csr *A, bool need_cols) {
   if ((reinterpret_cast<uintptr_t>(A->row_ptr) | reinterpret_cast<uintptr_t>(A->col_idx) |
        reinterpret_cast<uintptr_t>(A->vals)) & 3u)
     return fail(AUTOSAGE_ERR_INVALID_ARG, "CSR arrays must be 4-byte aligned");
-  (void)need_cols;
-  if (getenv("AUTOSAGE_CHECK") && atoi(getenv("AUTOSAGE_CHECK")) > 0) {
+  if (gpu_check && getenv("AUTOSAGE_CHECK") && atoi(getenv("AUTOSAGE_CHECK")) > 0) {
     // full structural check on the GPU (synchronising)
     autosage_status st = autosage_validate_csr(A, nullptr);
     if (st != AUTOSAGE_OK) return st;
@@ -253,17 +255,22 @@ struct autosage_plan_s {
   bool from_cache = false;
   int64_t maxdeg = -1;  // longest row of the walked CSR (-1: not computed)
   bool comp = true;     // SpMM: compensated accumulation (serial sums longer than 512 edges)
-  // the CSR the kernels walk (A, or A^T for SPMM_T)
+  // The A the plan is bound to: calls must pass these structure arrays (the
+  // edge values come from each call); a0 also serves the planning probes.
+  // a_fp is the fingerprint of A's structure (autosage_plan_rebind checks it).
+  autosage_csr a0{};
+  uint64_t a_fp = 0;
+  // the CSR the plan's workspace was built over (A, or A^T for SPMM_T)
   int64_t k_rows = 0;
   const int32_t *k_row_ptr = nullptr;
   const int32_t *k_col_idx = nullptr;
-  const float *k_vals = nullptr;
-  DevBuf t_row_ptr, t_col_idx, t_vals;  // A^T when op == SPMM_T
+  // A^T when op == SPMM_T; t_vals receives the call's edge values in A^T order
+  DevBuf t_row_ptr, t_col_idx, t_vals;
   // split workspace
   DevBuf long_rows, long_ptr, chunk_row, chunk_begin, partial, ml, row_ml, row_order;
   ChunkList cl;
   // merge-path workspace
-  DevBuf mp_part, mp_carry_val, mp_carry_row;
+  DevBuf mp_part, mp_carry_val, mp_carry_row, mp_head_val;
   int64_t mp_warps = 0;
   // unfused attention scores (backward: the softmax weights)
   DevBuf scores;
@@ -271,14 +278,18 @@ struct autosage_plan_s {
   // buffers (dW scratch, w and dS in A^T order) and the A^T SpMM plan
   DevBuf t_perm, t_inv, grad_dw, grad_wt, grad_dst;
   autosage_plan_s *tplan = nullptr;
-  // typed SpMM: number of relations (0: untyped) and the combined gather index
+  // typed SpMM: number of relations (0: untyped), the combined gather index,
+  // and the caller's column and edge-type arrays it was built from
   int typed = 0;
   int64_t base_cols = 0;
   DevBuf typed_idx;
+  const int32_t *typed_col = nullptr;
+  const int32_t *typed_type = nullptr;
   ~autosage_plan_s() {
     for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
                       &chunk_begin, &partial, &ml, &row_ml, &row_order, &mp_part, &mp_carry_val,
-                      &mp_carry_row, &scores, &t_perm, &t_inv, &grad_dw, &grad_wt, &grad_dst, &typed_idx})
+                      &mp_carry_row, &mp_head_val, &scores, &t_perm, &t_inv, &grad_dw, &grad_wt, &grad_dst,
+                      &typed_idx})
       b->release();
     delete tplan;
   }
@@ -404,6 +415,7 @@ autosage_status build_mergepath(autosage_plan_s *P, int items, int64_t width, cu
   CUDA_TRY(P->mp_part.alloc(sizeof(int2) * (size_t)(P->mp_warps + 1)));
   CUDA_TRY(P->mp_carry_val.alloc(sizeof(float) * (size_t)std::max<int64_t>(P->mp_warps * width, 1)));
   CUDA_TRY(P->mp_carry_row.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(P->mp_warps, 1)));
+  CUDA_TRY(P->mp_head_val.alloc(sizeof(float) * (size_t)std::max<int64_t>(P->mp_warps * width, 1)));
   CUDA_TRY(launch_mergepath_partition(P->k_rows, P->nnz, P->k_row_ptr, items, P->mp_warps,
                                       P->mp_part.as<int2>(), s));
   return AUTOSAGE_OK;
@@ -412,7 +424,8 @@ autosage_status build_mergepath(autosage_plan_s *P, int items, int64_t width, cu
 // Build the workspace of a schedule for plan P (P->sched set).
 autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
   for (DevBuf *b : {&P->long_rows, &P->long_ptr, &P->chunk_row, &P->chunk_begin, &P->partial,
-                    &P->ml, &P->row_ml, &P->row_order, &P->mp_part, &P->mp_carry_val, &P->mp_carry_row})
+                    &P->ml, &P->row_ml, &P->row_order, &P->mp_part, &P->mp_carry_val, &P->mp_carry_row,
+                    &P->mp_head_val})
     b->release();
   P->cl = ChunkList{};
   P->mp_warps = 0;
@@ -474,14 +487,38 @@ struct OpArgs {
   void *dQ = nullptr, *dK = nullptr, *dV = nullptr;
 };
 
-// Run `op` with plan P's schedule (plan-free runs use a transient P with
-// the default schedule and no workspace).
-autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a, cudaStream_t s) {
+// The CSR one call walks: the caller's row_ptr, col_idx and edge values;
+// for SPMM_T the plan's A^T, with the caller's edge values gathered into
+// A^T's edge order through the stored permutation (so new values take
+// effect without a new plan).
+struct Walk {
+  int64_t rows;
+  const int32_t *row_ptr;
+  const int32_t *col_idx;
+  const float *vals;
+};
+
+cudaError_t walk_for(const autosage_plan_s *P, autosage_op op, const autosage_csr *A, cudaStream_t s, Walk &w) {
+  if (op != AUTOSAGE_OP_SPMM_T) {
+    w = Walk{A->n_rows, A->row_ptr, A->col_idx, A->vals};
+    return cudaSuccess;
+  }
+  w = Walk{P->k_rows, P->k_row_ptr, P->k_col_idx, nullptr};
+  if (!A->vals || A->nnz == 0) return cudaSuccess;
+  w.vals = P->t_vals.as<float>();
+  return launch_gather_vals(A->nnz, P->t_perm.as<int32_t>(), A->vals, P->t_vals.as<float>(), s);
+}
+
+// Run `op` over the call's A with plan P's schedule (plan-free runs use a
+// transient P with the default schedule and no workspace).
+autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_csr *A, const OpArgs &a,
+                       cudaStream_t s) {
   const ChunkList &cl = P->cl;
-  const OpShape sh = op_shape(op, P->F, P->H);
   Geom g;
   autosage_status st;
-  cudaError_t e = cudaSuccess;
+  Walk wk;
+  cudaError_t e = walk_for(P, op, A, s, wk);
+  if (e != cudaSuccess) return cuda_fail(e, "edge values in A^T order");
   switch (op) {
     case AUTOSAGE_OP_SPMM:
     case AUTOSAGE_OP_SPMM_T: {
@@ -503,11 +540,11 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
         gt.comp = P->comp;
         if (mp) {
           gt.E = 32 / gt.G;
-          e = launch_spmm_mergepath(gt, P->k_rows, P->k_row_ptr, P->k_col_idx, P->k_vals, x, a.ldx, y,
+          e = launch_spmm_mergepath(gt, wk.rows, wk.row_ptr, wk.col_idx, wk.vals, x, a.ldx, y,
                                     a.ldy, P->mp_part.as<int2>(), P->mp_warps, P->mp_carry_val.as<float>(),
-                                    P->mp_carry_row.as<int32_t>(), s);
+                                    P->mp_carry_row.as<int32_t>(), P->mp_head_val.as<float>(), s);
         } else {
-          e = launch_spmm(gt, P->k_rows, P->k_row_ptr, P->k_col_idx, P->k_vals, x, a.ldx, y, a.ldy, cl,
+          e = launch_spmm(gt, wk.rows, wk.row_ptr, wk.col_idx, wk.vals, x, a.ldx, y, a.ldy, cl,
                           P->partial.as<float>(), s);
         }
       }
@@ -517,11 +554,11 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
       st = choose_geom(P->dt, 1, P->F, {{a.Q, a.ldq}, {a.K, a.ldk}}, P->sched.G, P->sched.E, true, 16, g);
       if (st != AUTOSAGE_OK) return st;
       if (P->sched.pe) g.batched = false;
-      e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.ldq, a.K, a.ldk, a.alpha, a.S, cl, s);
+      e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, a.ldq, a.K, a.ldk, a.alpha, a.S, cl, s);
       break;
     }
     case AUTOSAGE_OP_SOFTMAX: {
-      e = launch_row_softmax(P->k_rows, P->k_row_ptr, P->H, a.S, cl, P->ml.as<float>(),
+      e = launch_row_softmax(wk.rows, wk.row_ptr, P->H, a.S, cl, P->ml.as<float>(),
                              P->row_ml.as<float>(), s);
       break;
     }
@@ -534,7 +571,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
                          P->sched.E, true, 8, g);
       }
       if (st == AUTOSAGE_OK) {
-        e = launch_attention(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.K, a.given, a.X, ld, a.alpha,
+        e = launch_attention(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, a.K, a.given, a.X, ld, a.alpha,
                              a.Y, cl, P->partial.as<float>(), P->ml.as<float>(), s);
         break;
       }
@@ -548,7 +585,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
                          P->sched.G, P->sched.E, true, 8, g);
         if (st != AUTOSAGE_OK) return st;
         g.es = P->H;
-        e = launch_attention(g, P->k_rows, P->k_row_ptr, P->k_col_idx, at(a.Q), at(a.K),
+        e = launch_attention(g, wk.rows, wk.row_ptr, wk.col_idx, at(a.Q), at(a.K),
                              a.given ? a.given + h : nullptr, at(a.X), ld, a.alpha,
                              const_cast<char *>(at(a.Y)), cl, P->partial.as<float>(), P->ml.as<float>(), s);
       }
@@ -559,7 +596,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
       float *S = a.S;
       st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}}, P->sched.G, P->sched.E, true, 16, g);
       if (st == AUTOSAGE_OK) {
-        e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, ld, a.K, ld, a.alpha, S, cl, s);
+        e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, ld, a.K, ld, a.alpha, S, cl, s);
       } else if (st == AUTOSAGE_ERR_UNSUPPORTED && P->H > 1) {
         const size_t es = dtype_size(P->dt);
         for (int h = 0; h < P->H && e == cudaSuccess; ++h) {
@@ -568,18 +605,18 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
           st = choose_geom(P->dt, 1, P->F, {{q, ld}, {k, ld}}, P->sched.G, P->sched.E, true, 16, g);
           if (st != AUTOSAGE_OK) return st;
           g.es = P->H;
-          e = launch_sddmm(g, P->k_rows, P->k_row_ptr, P->k_col_idx, q, ld, k, ld, a.alpha, S + h, cl, s);
+          e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, q, ld, k, ld, a.alpha, S + h, cl, s);
         }
       } else {
         return st;
       }
       if (e != cudaSuccess) break;
-      e = launch_row_softmax(P->k_rows, P->k_row_ptr, P->H, S, cl, P->ml.as<float>(), P->row_ml.as<float>(), s);
+      e = launch_row_softmax(wk.rows, wk.row_ptr, P->H, S, cl, P->ml.as<float>(), P->row_ml.as<float>(), s);
       if (e != cudaSuccess) break;
       Geom g2;
       st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, P->sched.G, P->sched.E, false, 16, g2);
       if (st != AUTOSAGE_OK) return st;
-      e = launch_spmm(g2, P->k_rows, P->k_row_ptr, P->k_col_idx, S, a.X, ld, a.Y, ld, cl,
+      e = launch_spmm(g2, wk.rows, wk.row_ptr, wk.col_idx, S, a.X, ld, a.Y, ld, cl,
                       P->partial.as<float>(), s);
       break;
     }
@@ -592,7 +629,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const OpArgs &a
       st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}, {a.X, ld}, {a.dO, ld}, {a.dQ, ld}},
                        P->sched.G, P->sched.E, true, 8, g);
       if (st != AUTOSAGE_OK) return st;
-      e = launch_attention_backward(g, P->k_rows, P->k_row_ptr, P->k_col_idx, a.Q, a.K, a.X, a.dO, ld, P->H,
+      e = launch_attention_backward(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, a.K, a.X, a.dO, ld, P->H,
                                     a.alpha, a.dQ, P->scores.as<float>(), P->grad_dw.as<float>(),
                                     P->t_inv.as<int32_t>(), P->grad_wt.as<float>(), P->grad_dst.as<float>(), cl,
                                     P->partial.as<float>(), P->row_ml.as<float>(), s);
@@ -701,18 +738,25 @@ autosage_status make_plan_shell(const autosage_csr *A, autosage_op op, int64_t F
   P->n_rows = A->n_rows;
   P->n_cols = A->n_cols;
   P->nnz = A->nnz;
+  P->a0 = *A;
+  st = autosage_fingerprint(A, &P->a_fp, s);
+  if (st != AUTOSAGE_OK) {
+    delete P;
+    return st;
+  }
   P->k_rows = A->n_rows;
   P->k_row_ptr = A->row_ptr;
   P->k_col_idx = A->col_idx;
-  P->k_vals = A->vals;
   if (op == AUTOSAGE_OP_SPMM_T) {
+    // the structure of A^T and the permutation that carries each call's
+    // edge values into A^T's order
     cudaError_t e = P->t_row_ptr.alloc(sizeof(int32_t) * (size_t)(A->n_cols + 1));
     if (e == cudaSuccess) e = P->t_col_idx.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(A->nnz, 1));
-    if (e == cudaSuccess && A->vals) e = P->t_vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(A->nnz, 1));
+    if (e == cudaSuccess) e = P->t_vals.alloc(sizeof(float) * (size_t)std::max<int64_t>(A->nnz, 1));
     if (e == cudaSuccess) e = P->t_perm.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(A->nnz, 1));
     if (e == cudaSuccess)
-      e = csr_transpose(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx, A->vals,
-                        P->t_row_ptr.as<int32_t>(), P->t_col_idx.as<int32_t>(), P->t_vals.as<float>(),
+      e = csr_transpose(A->n_rows, A->n_cols, A->nnz, A->row_ptr, A->col_idx, nullptr,
+                        P->t_row_ptr.as<int32_t>(), P->t_col_idx.as<int32_t>(), nullptr,
                         P->t_perm.as<int32_t>(), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
@@ -722,7 +766,6 @@ autosage_status make_plan_shell(const autosage_csr *A, autosage_op op, int64_t F
     P->k_rows = A->n_cols;
     P->k_row_ptr = P->t_row_ptr.as<int32_t>();
     P->k_col_idx = P->t_col_idx.as<int32_t>();
-    P->k_vals = A->vals ? P->t_vals.as<float>() : nullptr;
   }
   *out = P;
   return AUTOSAGE_OK;
@@ -820,7 +863,7 @@ autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &
       cudaMemcpyAsync(pb.Y.p, pb.S.p, (size_t)pb.out_elems * 4, cudaMemcpyDeviceToDevice, s);
     if (pb.flush.p) cudaMemsetAsync(pb.flush.p, r & 0xff, pb.flush.bytes, s);
     cudaEventRecord(e0, s);
-    st = run_op(P, P->op, a, s);
+    st = run_op(P, P->op, &P->a0, a, s);
     cudaEventRecord(e1, s);
     cudaError_t e = cudaEventSynchronize(e1);
     if (e != cudaSuccess) st = cuda_fail(e, "probe");
@@ -999,9 +1042,8 @@ autosage_status build_backward_plan(autosage_plan_s *P, const Sched &sc, cudaStr
   if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) P->sched = Sched{AUTOSAGE_SCHED_SPLIT, sc.G, sc.E, sc.split};
   autosage_status st = build_workspace(P, s);
   if (st != AUTOSAGE_OK) return st;
-  autosage_csr A{P->n_rows, P->n_cols, P->nnz, P->k_row_ptr, P->k_col_idx, P->k_vals};
   autosage_plan_s *T = nullptr;
-  st = make_plan_shell(&A, AUTOSAGE_OP_SPMM_T, P->F * P->H, 1, static_cast<autosage_dtype>(P->dt), &T, s);
+  st = make_plan_shell(&P->a0, AUTOSAGE_OP_SPMM_T, P->F * P->H, 1, static_cast<autosage_dtype>(P->dt), &T, s);
   if (st != AUTOSAGE_OK) return st;
   T->sched = Sched{P->sched.kind, 0, 0, P->sched.split};
   st = build_workspace(T, s);
@@ -1112,10 +1154,10 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
     delete P;
     return st;
   }
-  uint64_t fp = 0;
-  {
-    autosage_csr K{P->k_rows, (op == AUTOSAGE_OP_SPMM_T) ? A->n_rows : A->n_cols, P->nnz,
-                   P->k_row_ptr, P->k_col_idx, P->k_vals};
+  // the cache key holds the fingerprint of the walked CSR (A^T for SPMM_T)
+  uint64_t fp = P->a_fp;
+  if (op == AUTOSAGE_OP_SPMM_T) {
+    autosage_csr K{P->k_rows, A->n_rows, P->nnz, P->k_row_ptr, P->k_col_idx, nullptr};
     st = autosage_fingerprint(&K, &fp, stream);
     if (st != AUTOSAGE_OK) {
       delete P;
@@ -1195,7 +1237,7 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
         if (op == AUTOSAGE_OP_ATTN_UNFUSED) a.S = P->scores.as<float>();
         if (op == AUTOSAGE_OP_SOFTMAX)
           cudaMemcpyAsync(pb.Y.p, pb.S.p, (size_t)pb.out_elems * 4, cudaMemcpyDeviceToDevice, s);
-        if (run_op(P, op, a, s) == AUTOSAGE_OK && cudaStreamSynchronize(s) == cudaSuccess) {
+        if (run_op(P, op, &P->a0, a, s) == AUTOSAGE_OK && cudaStreamSynchronize(s) == cudaSuccess) {
           const size_t bytes = (size_t)pb.out_elems * (pb.out_is_S ? 4 : dtype_size(P->dt));
           have_ref = cudaMemcpyAsync(pb.Y2.p, pb.Y.p, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
         }
@@ -1327,15 +1369,55 @@ autosage_status autosage_plan_schedule(autosage_plan_t P, autosage_schedule *sch
   return AUTOSAGE_OK;
 }
 
+autosage_status autosage_plan_rebind(autosage_plan_t P, const autosage_csr *A, void *stream) {
+  if (!P) return fail(AUTOSAGE_ERR_INVALID_ARG, "plan is NULL");
+  autosage_status st = check_csr(A, true);
+  if (st != AUTOSAGE_OK) return st;
+  if (P->typed) return fail(AUTOSAGE_ERR_UNSUPPORTED, "typed plans cannot be rebound; build a new one");
+  if (P->n_rows != A->n_rows || P->n_cols != A->n_cols || P->nnz != A->nnz)
+    return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for a graph of another size");
+  uint64_t fp = 0;
+  if ((st = autosage_fingerprint(A, &fp, stream)) != AUTOSAGE_OK) return st;
+  if (fp != P->a_fp) return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "A has another structure than the plan's graph");
+  P->a0 = *A;
+  if (P->op != AUTOSAGE_OP_SPMM_T) {
+    P->k_row_ptr = A->row_ptr;
+    P->k_col_idx = A->col_idx;
+  }
+  return AUTOSAGE_OK;
+}
+
 // ---------------------------------------------------------------- ops
 
+static bool check_mode() {
+  const char *c = getenv("AUTOSAGE_CHECK");
+  return c && atoi(c) > 0;
+}
+
+// A plan's workspace (chunk lists, row order, A^T, merge-path partitions) is
+// derived from the structure of the A it was built for, so a call must pass
+// the same row_ptr and col_idx arrays; the edge values are read from the call.
+// In checked mode the structure's fingerprint is compared as well, which
+// catches arrays that were overwritten in place with another graph.
 static autosage_status plan_matches(const autosage_plan_s *P, const autosage_csr *A, autosage_op op,
-                                    int64_t F, int H, autosage_dtype dt) {
+                                    int64_t F, int H, autosage_dtype dt, void *stream) {
   if (P->op != op) return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for op %d, called as op %d", (int)P->op, (int)op);
+  if (P->typed) return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "a typed plan runs only through autosage_spmm_typed");
   if (P->n_rows != A->n_rows || P->n_cols != A->n_cols || P->nnz != A->nnz)
     return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for another graph");
   if (P->F != F || P->H != H || (int)P->dt != (int)dt)
     return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan built for another width, head count or dtype");
+  if (A->row_ptr != P->a0.row_ptr || (A->nnz > 0 && A->col_idx != P->a0.col_idx))
+    return fail(AUTOSAGE_ERR_PLAN_MISMATCH,
+                "row_ptr / col_idx are not the arrays the plan was built for (after moving or copying the "
+                "structure, call autosage_plan_rebind)");
+  if (check_mode()) {
+    uint64_t fp = 0;
+    autosage_status st = autosage_fingerprint(A, &fp, stream);
+    if (st != AUTOSAGE_OK) return st;
+    if (fp != P->a_fp)
+      return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "the structure arrays changed since the plan was built");
+  }
   return AUTOSAGE_OK;
 }
 
@@ -1349,10 +1431,10 @@ static autosage_plan_s transient(const autosage_csr *A, autosage_op op, int64_t 
   P.n_rows = A->n_rows;
   P.n_cols = A->n_cols;
   P.nnz = A->nnz;
+  P.a0 = *A;
   P.k_rows = A->n_rows;
   P.k_row_ptr = A->row_ptr;
   P.k_col_idx = A->col_idx;
-  P.k_vals = A->vals;
   P.sched = default_sched();
   return P;
 }
@@ -1379,12 +1461,12 @@ autosage_status autosage_spmm(const autosage_csr *A, const void *X, int64_t ldx,
   a.X = X; a.ldx = ldx; a.Y = Y; a.ldy = ldy;
   const autosage_op op = transpose ? AUTOSAGE_OP_SPMM_T : AUTOSAGE_OP_SPMM;
   if (plan) {
-    if ((st = plan_matches(plan, A, op, F, 1, dt)) != AUTOSAGE_OK) return st;
-    return run_op(plan, op, a, as_stream(stream));
+    if ((st = plan_matches(plan, A, op, F, 1, dt, stream)) != AUTOSAGE_OK) return st;
+    return run_op(plan, op, A, a, as_stream(stream));
   }
   if (transpose) return fail(AUTOSAGE_ERR_INVALID_ARG, "transpose needs a plan built for AUTOSAGE_OP_SPMM_T");
   autosage_plan_s P = transient(A, op, F, 1, dt);
-  return run_op(&P, op, a, as_stream(stream));
+  return run_op(&P, op, A, a, as_stream(stream));
 }
 
 autosage_status autosage_sddmm(const autosage_csr *A, const void *Q, int64_t ldq, const void *K, int64_t ldk,
@@ -1401,16 +1483,16 @@ autosage_status autosage_sddmm(const autosage_csr *A, const void *Q, int64_t ldq
   OpArgs a;
   a.Q = Q; a.ldq = ldq; a.K = K; a.ldk = ldk; a.alpha = alpha; a.S = out;
   if (plan) {
-    if ((st = plan_matches(plan, A, AUTOSAGE_OP_SDDMM, F, 1, dt)) != AUTOSAGE_OK) return st;
-    return run_op(plan, AUTOSAGE_OP_SDDMM, a, as_stream(stream));
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_SDDMM, F, 1, dt, stream)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_SDDMM, A, a, as_stream(stream));
   }
   autosage_plan_s P = transient(A, AUTOSAGE_OP_SDDMM, F, 1, dt);
-  return run_op(&P, AUTOSAGE_OP_SDDMM, a, as_stream(stream));
+  return run_op(&P, AUTOSAGE_OP_SDDMM, A, a, as_stream(stream));
 }
 
 autosage_status autosage_row_softmax(const autosage_csr *A, float *scores, int heads, autosage_plan_t plan,
                                      void *stream) {
-  autosage_status st = check_csr(A, false);
+  autosage_status st = check_csr(A, true);
   if (st != AUTOSAGE_OK) return st;
   if (heads < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads must be >= 1");
   if (A->nnz > 0 && !scores) return fail(AUTOSAGE_ERR_INVALID_ARG, "scores is NULL");
@@ -1418,11 +1500,11 @@ autosage_status autosage_row_softmax(const autosage_csr *A, float *scores, int h
   OpArgs a;
   a.S = scores;
   if (plan) {
-    if ((st = plan_matches(plan, A, AUTOSAGE_OP_SOFTMAX, 1, heads, AUTOSAGE_F32)) != AUTOSAGE_OK) return st;
-    return run_op(plan, AUTOSAGE_OP_SOFTMAX, a, as_stream(stream));
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_SOFTMAX, 1, heads, AUTOSAGE_F32, stream)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_SOFTMAX, A, a, as_stream(stream));
   }
   autosage_plan_s P = transient(A, AUTOSAGE_OP_SOFTMAX, 1, heads, AUTOSAGE_F32);
-  return run_op(&P, AUTOSAGE_OP_SOFTMAX, a, as_stream(stream));
+  return run_op(&P, AUTOSAGE_OP_SOFTMAX, A, a, as_stream(stream));
 }
 
 autosage_status autosage_csr_attention(const autosage_csr *A, const void *Q, const void *K, const void *V,
@@ -1443,17 +1525,17 @@ autosage_status autosage_csr_attention(const autosage_csr *A, const void *Q, con
   cudaStream_t s = as_stream(stream);
   const autosage_op op = fused ? AUTOSAGE_OP_ATTN : AUTOSAGE_OP_ATTN_UNFUSED;
   if (plan) {
-    if ((st = plan_matches(plan, A, op, D, heads, dt)) != AUTOSAGE_OK) return st;
+    if ((st = plan_matches(plan, A, op, D, heads, dt, stream)) != AUTOSAGE_OK) return st;
     if (!fused) a.S = plan->scores.as<float>();
-    return run_op(plan, op, a, s);
+    return run_op(plan, op, A, a, s);
   }
   autosage_plan_s P = transient(A, op, D, heads, dt);
-  if (fused) return run_op(&P, op, a, s);
+  if (fused) return run_op(&P, op, A, a, s);
   float *S = nullptr;
   cudaError_t e = cudaMallocAsync(&S, sizeof(float) * (size_t)std::max<int64_t>(A->nnz * heads, 1), s);
   if (e != cudaSuccess) return cuda_fail(e, "score buffer");
   a.S = S;
-  st = run_op(&P, op, a, s);
+  st = run_op(&P, op, A, a, s);
   cudaFreeAsync(S, s);
   return st;
 }
@@ -1473,11 +1555,11 @@ autosage_status autosage_edge_softmax_aggregate(const autosage_csr *A, const flo
   OpArgs a;
   a.X = V; a.Y = out; a.given = scores;
   if (plan) {
-    if ((st = plan_matches(plan, A, AUTOSAGE_OP_ATTN, D, heads, dt)) != AUTOSAGE_OK) return st;
-    return run_op(plan, AUTOSAGE_OP_ATTN, a, as_stream(stream));
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_ATTN, D, heads, dt, stream)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_ATTN, A, a, as_stream(stream));
   }
   autosage_plan_s P = transient(A, AUTOSAGE_OP_ATTN, D, heads, dt);
-  return run_op(&P, AUTOSAGE_OP_ATTN, a, as_stream(stream));
+  return run_op(&P, AUTOSAGE_OP_ATTN, A, a, as_stream(stream));
 }
 
 autosage_status autosage_csr_attention_backward(const autosage_csr *A, const void *Q, const void *K,
@@ -1501,14 +1583,14 @@ autosage_status autosage_csr_attention_backward(const autosage_csr *A, const voi
   a.Q = Q; a.K = K; a.X = V; a.dO = dO; a.dQ = dQ; a.dK = dK; a.dV = dV; a.alpha = scale;
   cudaStream_t s = as_stream(stream);
   if (plan) {
-    if ((st = plan_matches(plan, A, AUTOSAGE_OP_ATTN_BACKWARD, D, heads, dt)) != AUTOSAGE_OK) return st;
-    return run_op(plan, AUTOSAGE_OP_ATTN_BACKWARD, a, s);
+    if ((st = plan_matches(plan, A, AUTOSAGE_OP_ATTN_BACKWARD, D, heads, dt, stream)) != AUTOSAGE_OK) return st;
+    return run_op(plan, AUTOSAGE_OP_ATTN_BACKWARD, A, a, s);
   }
   autosage_plan_s *P = nullptr;
   st = make_plan_shell(A, AUTOSAGE_OP_ATTN_BACKWARD, D, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
   st = build_backward_plan(P, default_backward_sched(), s);
-  if (st == AUTOSAGE_OK) st = run_op(P, AUTOSAGE_OP_ATTN_BACKWARD, a, s);
+  if (st == AUTOSAGE_OK) st = run_op(P, AUTOSAGE_OP_ATTN_BACKWARD, A, a, s);
   cudaError_t e = cudaStreamSynchronize(s);
   delete P;
   if (st == AUTOSAGE_OK && e != cudaSuccess) return cuda_fail(e, "attention backward");
@@ -1555,6 +1637,8 @@ autosage_status autosage_plan_typed(const autosage_csr *A, const int32_t *edge_t
   P->typed_idx = idx;  // the plan owns the index from here on
   idx.p = nullptr;
   idx.bytes = 0;
+  P->typed_col = A->col_idx;
+  P->typed_type = edge_type;
   *out = P;
   return st;
 }
@@ -1576,11 +1660,27 @@ autosage_status autosage_spmm_typed(const autosage_csr *A, const int32_t *edge_t
     if (plan->typed != num_types || plan->base_cols != A->n_cols || plan->n_rows != A->n_rows ||
         plan->nnz != A->nnz || plan->F != F || (int)plan->dt != (int)dt || plan->op != AUTOSAGE_OP_SPMM)
       return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "plan not built by autosage_plan_typed for this call");
-    return run_op(plan, AUTOSAGE_OP_SPMM, a, s);
+    // the combined gather index was built from these arrays: they are structure
+    if (A->row_ptr != plan->a0.row_ptr || (A->nnz > 0 && (A->col_idx != plan->typed_col || edge_type != plan->typed_type)))
+      return fail(AUTOSAGE_ERR_PLAN_MISMATCH,
+                  "row_ptr / col_idx / edge_type are not the arrays the typed plan was built from");
+    // the stacked relation blocks as one CSR: the plan's combined index, the call's values
+    const autosage_csr Ap{A->n_rows, (int64_t)num_types * A->n_cols, A->nnz, A->row_ptr,
+                          plan->typed_idx.as<int32_t>(), A->vals};
+    if (check_mode()) {
+      uint64_t fp = 0;
+      if ((st = autosage_fingerprint(&Ap, &fp, stream)) != AUTOSAGE_OK) return st;
+      if (fp != plan->a_fp) return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "the structure arrays changed since the plan was built");
+    }
+    return run_op(plan, AUTOSAGE_OP_SPMM, &Ap, a, s);
   }
   autosage_plan_t P = nullptr;
   st = autosage_plan_typed(A, edge_type, num_types, F, dt, AUTOSAGE_PLAN_NO_CACHE, &P, stream);
-  if (st == AUTOSAGE_OK) st = run_op(P, AUTOSAGE_OP_SPMM, a, s);
+  if (st == AUTOSAGE_OK) {
+    const autosage_csr Ap{A->n_rows, (int64_t)num_types * A->n_cols, A->nnz, A->row_ptr,
+                          P->typed_idx.as<int32_t>(), A->vals};
+    st = run_op(P, AUTOSAGE_OP_SPMM, &Ap, a, s);
+  }
   cudaError_t e = cudaStreamSynchronize(s);
   autosage_plan_destroy(P);
   if (st == AUTOSAGE_OK && e != cudaSuccess) return cuda_fail(e, "typed SpMM");
@@ -1753,26 +1853,32 @@ autosage_status report(autosage_status st, const char *msg) { return fail(st, "%
 
 // Unfused CSR attention with a caller-supplied fp32 score buffer of at least
 // nnz * heads elements, default schedule, no plan, no device allocation.
+// check_attention_args runs the same host-side checks as
+// autosage_csr_attention (no GPU work, so no allocation: the structural
+// validation of AUTOSAGE_CHECK is left out); attention_unfused_with_scores
+// launches the three kernels on arguments that passed it.
 namespace autosage {
-autosage_status attention_unfused_with_scores(const autosage_csr *A, const void *Q, const void *K,
-                                              const void *V, int heads, int64_t D, autosage_dtype dt,
-                                              float scale, void *out, float *scores, cudaStream_t s) {
-  if (!A) return fail(AUTOSAGE_ERR_INVALID_ARG, "A is NULL");
-  if (A->n_rows < 0 || A->n_cols < 0 || A->nnz < 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "negative CSR size");
-  if (!A->row_ptr || (A->nnz > 0 && !A->col_idx)) return fail(AUTOSAGE_ERR_INVALID_ARG, "CSR pointer is NULL");
-  if (A->nnz > 0 && A->n_cols == 0) return fail(AUTOSAGE_ERR_INVALID_CSR, "edges but no columns");
+autosage_status check_attention_args(const autosage_csr *A, const void *Q, const void *K, const void *V, int heads,
+                                     int64_t D, autosage_dtype dt, const void *out) {
+  autosage_status st = check_csr(A, false);
+  if (st != AUTOSAGE_OK) return st;
   if (heads < 1 || D < 1) return fail(AUTOSAGE_ERR_INVALID_ARG, "heads and D must be >= 1");
   if (dt != AUTOSAGE_F32 && dt != AUTOSAGE_BF16) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad dtype");
   const int64_t W = (int64_t)heads * D;
-  autosage_status st;
   if ((st = check_mat(Q, W, W, A->n_rows, "Q")) != AUTOSAGE_OK) return st;
   if ((st = check_mat(K, W, W, A->n_cols, "K")) != AUTOSAGE_OK) return st;
   if ((st = check_mat(V, W, W, A->n_cols, "V")) != AUTOSAGE_OK) return st;
   if ((st = check_mat(out, W, W, A->n_rows, "out")) != AUTOSAGE_OK) return st;
+  return AUTOSAGE_OK;
+}
+
+autosage_status attention_unfused_with_scores(const autosage_csr *A, const void *Q, const void *K,
+                                              const void *V, int heads, int64_t D, autosage_dtype dt,
+                                              float scale, void *out, float *scores, cudaStream_t s) {
   if (A->n_rows == 0) return AUTOSAGE_OK;
   OpArgs a;
   a.Q = Q; a.K = K; a.X = V; a.Y = out; a.alpha = scale; a.S = scores;
   autosage_plan_s P = transient(A, AUTOSAGE_OP_ATTN_UNFUSED, D, heads, dt);
-  return run_op(&P, AUTOSAGE_OP_ATTN_UNFUSED, a, s);
+  return run_op(&P, AUTOSAGE_OP_ATTN_UNFUSED, A, a, s);
 }
 }  // namespace autosage

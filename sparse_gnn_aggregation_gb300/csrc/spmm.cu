@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const float *__restrict__ vals, const T *__restrict__ X, int64_t ldx, T *__restrict__ Y,
     int64_t ldy, int nfrag, int G, int E, const int2 *__restrict__ part, int64_t n_warps,
-    float *__restrict__ carry_val, int32_t *__restrict__ carry_row) {
+    float *__restrict__ carry_val, int32_t *__restrict__ carry_row, float *__restrict__ head_val) {
   const int64_t w = (int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5);
   if (w >= n_warps) return;  // whole warps leave together
   const Lanes L(G, E);       // G * E == 32: one group per warp
@@ -245,7 +245,15 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
     gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, true, head, X, ldx, nfrag, frag, E, b + L.e, e, acc,
                                      comp);
     reduce_edge_lanes(acc, FULL, G, 32);
-    if (L.e == 0) {
+    if (L.e != 0) continue;
+    if (i == s0.x && row_ptr[i] < s0.y) {
+      // the last segment of a row that earlier warps began: kept in fp32 for
+      // the fix-up, which adds the carries and rounds the row once
+      float *hv = head_val + w * (int64_t)nfrag * VW;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (L.g + k * G < nfrag) store_partial<VW>(hv + (int64_t)(L.g + k * G) * VW, acc[k]);
+    } else {
       T *y = Y + (int64_t)i * ldy;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
@@ -276,11 +284,13 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
 }
 
 // The first warp carrying a row adds every carry of that row (in warp order)
-// to the value the row's finishing warp wrote.
+// and then the fp32 segment of the row's finishing warp (the warp after the
+// last carry), and rounds the sum to T once.
 template <typename T, int VW>
 __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
     int64_t n_warps, int nfrag, const float *__restrict__ carry_val,
-    const int32_t *__restrict__ carry_row, T *__restrict__ Y, int64_t ldy) {
+    const int32_t *__restrict__ carry_row, const float *__restrict__ head_val, T *__restrict__ Y,
+    int64_t ldy) {
   const int64_t w = (int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5);
   if (w >= n_warps) return;
   const int r = carry_row[w];
@@ -294,17 +304,19 @@ __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
     float comp[VW];
 #pragma unroll
     for (int v = 0; v < VW; ++v) comp[v] = 0.f;
-    for (int64_t q = w; q < n_warps && carry_row[q] == r; ++q) {
+    int64_t q = w;
+    for (; q < n_warps && carry_row[q] == r; ++q) {
       const float *src = carry_val + q * F + (int64_t)f * VW;
 #pragma unroll
       for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, __ldcg(src + v));
     }
-    T *y = Y + (int64_t)r * ldy + (int64_t)f * VW;
-    Frag<T, VW> cur;
-    cur.load(y);
+    // warp q finishes row r (a carried row always ends in a later warp, so q < n_warps)
+    if (q < n_warps) {
+      const float *hv = head_val + q * F + (int64_t)f * VW;
 #pragma unroll
-    for (int v = 0; v < VW; ++v) acc[v] += cur.get(v);
-    store_frag<T, VW>(y, acc);
+      for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, __ldcg(hv + v));
+    }
+    store_frag<T, VW>(Y + (int64_t)r * ldy + (int64_t)f * VW, acc);
   }
 }
 
@@ -351,13 +363,13 @@ template <typename T, int VW>
 cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const float *vals, const T *X, int64_t ldx, T *Y,
                          int64_t ldy, const int2 *part, int64_t n_warps, float *carry_val,
-                         int32_t *carry_row, cudaStream_t s) {
+                         int32_t *carry_row, float *head_val, cudaStream_t s) {
   if (n_warps <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_warps + kBlock / 32 - 1) / (kBlock / 32));
 #define AUTOSAGE_MP_K(NVV, CMP)                                                                    \
   spmm_mergepath_kernel<T, VW, NVV, CMP><<<grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, vals, X,  \
                                                                 ldx, Y, ldy, g.nfrag, g.G, g.E,     \
-                                                                part, n_warps, carry_val, carry_row)
+                                                                part, n_warps, carry_val, carry_row, head_val)
 #define AUTOSAGE_MP_NV(NVV)           \
   if (g.comp) AUTOSAGE_MP_K(NVV, true); \
   else AUTOSAGE_MP_K(NVV, false);
@@ -373,7 +385,7 @@ cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
 #undef AUTOSAGE_MP_K
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  mergepath_fixup_kernel<T, VW><<<grid, kBlock, 0, s>>>(n_warps, g.nfrag, carry_val, carry_row, Y, ldy);
+  mergepath_fixup_kernel<T, VW><<<grid, kBlock, 0, s>>>(n_warps, g.nfrag, carry_val, carry_row, head_val, Y, ldy);
   return cudaGetLastError();
 }
 
@@ -416,24 +428,24 @@ cudaError_t launch_spmm_mergepath(const Geom &g, int64_t n_rows, const int32_t *
                                   const int32_t *col_idx, const float *vals, const void *X,
                                   int64_t ldx, void *Y, int64_t ldy, const int2 *part,
                                   int64_t n_warps, float *carry_val, int32_t *carry_row,
-                                  cudaStream_t s) {
+                                  float *head_val, cudaStream_t s) {
   if (g.G * g.E != 32) return cudaErrorInvalidValue;
   if (g.dt == DType::F32) {
     auto x = static_cast<const float *>(X);
     auto y = static_cast<float *>(Y);
     switch (g.VW) {
-      case 4: return mergepath_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
-      case 2: return mergepath_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
-      case 1: return mergepath_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 4: return mergepath_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 2: return mergepath_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 1: return mergepath_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
     }
   } else {
     auto x = static_cast<const __nv_bfloat16 *>(X);
     auto y = static_cast<__nv_bfloat16 *>(Y);
     switch (g.VW) {
-      case 8: return mergepath_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
-      case 4: return mergepath_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
-      case 2: return mergepath_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
-      case 1: return mergepath_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, s);
+      case 8: return mergepath_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 4: return mergepath_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 2: return mergepath_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 1: return mergepath_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
     }
   }
   return cudaErrorInvalidValue;

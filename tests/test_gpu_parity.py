@@ -117,6 +117,38 @@ def test_spmm_no_values_means_ones(skew):
     assert_close(to_np(sga.autosage_spmm(A, dev(X))), oracle.spmm(g.row_ptr, g.col_idx, None, X), TOL_F32)
 
 
+@pytest.mark.parametrize("items", [32, 300])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_spmm_mergepath_cut_row_rounded_once(items, bf16):
+    # One hub row cut by the merge path into many warps' segments: its first
+    # 1501 edges have value +1 and its last 1500 value -1 over identical X
+    # rows, so every warp's segment sums to hundreds of X rows while the row's
+    # exact result is one X row. The segments must be added in fp32 and the
+    # row rounded to the output type once; rounding the finishing segment to
+    # bf16 first would be off by up to (its length) * 2^-9.
+    k = 1500
+    n = 2 * k + 1
+    cols = np.arange(n, dtype=np.int32)
+    vals = np.concatenate([np.ones(k + 1), -np.ones(k)]).astype(np.float32)
+    row_ptr = np.array([0, n] + [n + i + 1 for i in range(n - 1)], dtype=np.int32)  # then one edge per row
+    col_idx = np.concatenate([cols, (np.arange(n - 1, dtype=np.int32) * 7) % n]).astype(np.int32)
+    vals = np.concatenate([vals, np.full(n - 1, 0.5, np.float32)])
+    g = synth.Csr(n, n, row_ptr, col_idx, vals)
+    F = 8
+    base = synth.normal(1, F, 17, synth.STREAM_X) * 3.0
+    X32 = np.repeat(base, n, axis=0)
+    if bf16:
+        Xd, X32 = bf16_tensor(X32)
+    else:
+        Xd = dev(X32)
+    A = mat(g)
+    plan = make_plan(A, sga.OP_SPMM, F, dict(kind=sga.SCHED_MERGEPATH, split=items))
+    Y = sga.autosage_spmm(A, Xd, plan=plan)
+    want = oracle.spmm(g.row_ptr, g.col_idx, g.vals, X32)
+    assert_close(to_np(Y), want, TOL_BF16 if bf16 else TOL_F32, f"merge path items={items} bf16={bf16}")
+    assert "chunks" in plan.describe()
+
+
 @pytest.mark.parametrize("name,spec", SPMM_SCHEDULES, ids=[s[0] for s in SPMM_SCHEDULES])
 def test_spmm_transpose(skew, name, spec):
     g = skew

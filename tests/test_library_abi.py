@@ -71,6 +71,31 @@ def test_host_side_argument_checks_need_no_gpu(lib_path):
                                            None) == sga.ERR_INVALID_ARG
 
 
+def test_no_alloc_entry_checks_its_csr_on_the_host(lib_path):
+    """The allocation-free attention refuses a misaligned or over-large CSR with
+    the same host-side checks as autosage_csr_attention, before it touches a
+    device (this runs without a GPU: a refused call makes no CUDA call)."""
+    import ctypes
+    import sparse_gnn_aggregation_gb300 as sga
+    lib = sga.library()
+    P = ctypes.c_void_p
+    feat = P(0x10000)  # stand-in device addresses: never dereferenced on a refused call
+    misaligned = sga._Csr(4, 4, 4, 0x20000, 0x30002, 0)  # col_idx not 4-byte aligned
+    st = lib.autosage_csr_attention_unfused_noalloc(ctypes.byref(misaligned), feat, feat, feat, 1, 4, sga.F32,
+                                                    1.0, feat, None)
+    assert st == sga.ERR_INVALID_ARG
+    assert b"aligned" in lib.autosage_last_error()
+    huge = sga._Csr(2 ** 31, 4, 4, 0x20000, 0x30000, 0)  # n_rows does not fit int32
+    st = lib.autosage_csr_attention_unfused_noalloc(ctypes.byref(huge), feat, feat, feat, 1, 4, sga.F32,
+                                                    1.0, feat, None)
+    assert st == sga.ERR_UNSUPPORTED
+    ok = sga._Csr(4, 4, 4, 0x20000, 0x30000, 0)
+    st = lib.autosage_csr_attention_unfused_noalloc(ctypes.byref(ok), feat, feat, feat, 0, 4, sga.F32,
+                                                    1.0, feat, None)
+    assert st == sga.ERR_INVALID_ARG  # heads < 1
+    assert lib.autosage_plan_rebind(None, ctypes.byref(ok), None) == sga.ERR_INVALID_ARG
+
+
 def test_header_is_plain_c_and_a_c_program_links(lib_path, tmp_path):
     # the boundary is usable from C: the header compiles as C11 (no C++ or
     # torch types), and a C program links against the library and calls the

@@ -305,6 +305,25 @@ def test_attention_matches_dense_masked(name, kw, heads):
     np.testing.assert_allclose(O, dense_attention(rp, ci, Q, K, V, heads, 0.5), rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("heads", [1, 2])
+def test_attention_duplicate_edges_are_separate_terms(heads):
+    # Reading of the CSR with repeated entries: each entry is its own term of
+    # the row's softmax and sum (a repeated edge counts twice). Expanding the
+    # columns so that entry p of the CSR is key/value column p turns the
+    # pattern into one without repeats, where dense masked attention applies.
+    rp, ci, _ = random_csr(n_rows=12, n_cols=9, density=0.5, seed=3, dup=True)
+    assert any(np.unique(ci[rp[i]:rp[i + 1]]).size < rp[i + 1] - rp[i] for i in range(12)), "no repeated entry"
+    rng = np.random.default_rng(15)
+    D = 4
+    Q = rng.standard_normal((12, heads * D)).astype(np.float32)
+    K = rng.standard_normal((9, heads * D)).astype(np.float32)
+    V = rng.standard_normal((9, heads * D)).astype(np.float32)
+    O = oracle.csr_attention(rp, ci, Q, K, V, heads, 0.5)
+    expanded = np.arange(ci.size, dtype=np.int32)
+    want = dense_attention(rp, expanded, Q, K[ci], V[ci], heads, 0.5)
+    np.testing.assert_allclose(O, want, rtol=1e-12, atol=1e-13)
+
+
 def test_attention_constant_scores_is_mean_aggregation():
     g = synth.erdos_renyi(64, 6.0, seed=3)
     rng = np.random.default_rng(5)
