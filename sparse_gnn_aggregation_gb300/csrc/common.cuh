@@ -75,6 +75,7 @@ template <> struct Frag<float, 1> {
 };
 template <> struct Frag<__nv_bfloat16, 8> {
   uint4 r;
+  __device__ __forceinline__ uint32_t word(int i) const { return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w; }
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const uint4 *>(p)); }
   __device__ __forceinline__ void zero() { r = make_uint4(0u, 0u, 0u, 0u); }
   __device__ __forceinline__ float get(int i) const {
@@ -88,6 +89,7 @@ template <> struct Frag<__nv_bfloat16, 8> {
 };
 template <> struct Frag<__nv_bfloat16, 4> {
   uint2 r;
+  __device__ __forceinline__ uint32_t word(int i) const { return i == 0 ? r.x : r.y; }
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const uint2 *>(p)); }
   __device__ __forceinline__ void zero() { r = make_uint2(0u, 0u); }
   __device__ __forceinline__ float get(int i) const {
@@ -101,6 +103,7 @@ template <> struct Frag<__nv_bfloat16, 4> {
 };
 template <> struct Frag<__nv_bfloat16, 2> {
   uint32_t r;
+  __device__ __forceinline__ uint32_t word(int) const { return r; }
   __device__ __forceinline__ void load(const __nv_bfloat16 *p) { r = __ldg(reinterpret_cast<const unsigned int *>(p)); }
   __device__ __forceinline__ void zero() { r = 0u; }
   __device__ __forceinline__ float get(int i) const { return (i & 1) ? bf16hi(r) : bf16lo(r); }
@@ -157,6 +160,40 @@ __device__ __forceinline__ float frag_dot(const Frag<T, VW> &a, const Frag<T, VW
 #pragma unroll
     for (int i = 0; i < VW / 2; ++i) d = __ffma2_rn(a.get2(i), b.get2(i), d);
     return d.x + d.y;
+  } else {
+    return a.get(0) * b.get(0);
+  }
+}
+
+// a * b + c for the low (or high) bf16 halves of two packed words with the
+// mixed-precision FMA of sm_100 and later: the bf16 operands are multiplied
+// exactly and the sum rounded once in fp32, which is the value of widening
+// both halves to fp32 and calling fmaf, without the two widening steps.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// <a, b> over one bf16 fragment pair: even and odd elements in two chains
+// (the order of the packed-pair form above), added at the end.
+template <int VW>
+__device__ __forceinline__ float frag_dot(const Frag<__nv_bfloat16, VW> &a, const Frag<__nv_bfloat16, VW> &b) {
+  if constexpr (VW >= 2) {
+    float e = 0.f, o = 0.f;
+#pragma unroll
+    for (int i = 0; i < VW / 2; ++i) {
+      e = fma_bf16_lo(a.word(i), b.word(i), e);
+      o = fma_bf16_hi(a.word(i), b.word(i), o);
+    }
+    return e + o;
   } else {
     return a.get(0) * b.get(0);
   }

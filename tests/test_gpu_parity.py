@@ -142,11 +142,12 @@ def test_spmm_mergepath_cut_row_rounded_once(items, bf16):
     else:
         Xd = dev(X32)
     A = mat(g)
-    plan = make_plan(A, sga.OP_SPMM, F, dict(kind=sga.SCHED_MERGEPATH, split=items))
+    plan = make_plan(A, sga.OP_SPMM, F, dict(kind=sga.SCHED_MERGEPATH, split=items),
+                     dtype=torch.bfloat16 if bf16 else torch.float32)
     Y = sga.autosage_spmm(A, Xd, plan=plan)
     want = oracle.spmm(g.row_ptr, g.col_idx, g.vals, X32)
     assert_close(to_np(Y), want, TOL_BF16 if bf16 else TOL_F32, f"merge path items={items} bf16={bf16}")
-    assert "chunks" in plan.describe()
+    assert "sched=mergepath" in plan.describe()
 
 
 @pytest.mark.parametrize("name,spec", SPMM_SCHEDULES, ids=[s[0] for s in SPMM_SCHEDULES])
