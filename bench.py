@@ -181,8 +181,9 @@ def large_config_rows(dev, flush, stream, steps, warmup, oracle_frac=0.05):
     stream, algorithmic bytes), with the oracle timed beside each operation
     on a seeded uniform sample of the rows (fraction ``oracle_frac``):
       products-like (2,449,029 nodes, 123.7M edges, mean aggregation):
-        SpMM at F = 32 and 100, SpMM with A^T at F = 32 and 100, and the A^T
-        build (once per plan) on its own;
+        SpMM at F = 32 and 100, SpMM with A^T at F = 32 and 100 (fixed edge
+        values, kept in A^T order by the plan) and at F = 32 with the values
+        read per call (spmm_t_vpc), and the A^T build (once per plan) on its own;
       Reddit-like (232,965 nodes, 114.6M edges, 50 communities):
         SpMM at F = 128 and 602, SDDMM at F = 128."""
     import ctypes
@@ -214,7 +215,7 @@ def large_config_rows(dev, flush, stream, steps, warmup, oracle_frac=0.05):
 
     def oracle_rate(kind, g, F, X, gt=None):
         rng = np.random.default_rng(54321)
-        src = gt if kind == "spmm_t" else g
+        src = gt if kind.startswith("spmm_t") else g
         k = max(1, int(round(src.n_rows * oracle_frac)))
         rows = np.sort(rng.choice(src.n_rows, size=k, replace=False)).astype(np.int64)
         enn = int((src.row_ptr[rows + 1] - src.row_ptr[rows]).sum())
@@ -231,12 +232,12 @@ def large_config_rows(dev, flush, stream, steps, warmup, oracle_frac=0.05):
 
     flags = sga.PLAN_PROBE | sga.PLAN_VERIFY
     for gname, gen, ops in (("products", synth.products_like, [("spmm", 32), ("spmm", 100), ("spmm_t", 32),
-                                                               ("spmm_t", 100)]),
+                                                               ("spmm_t", 100), ("spmm_t_vpc", 32)]),
                             ("reddit", synth.reddit_like, [("spmm", 128), ("spmm", 602), ("sddmm", 128)])):
         g = gen(seed=0)
         A = sga.CsrMatrix.from_numpy(g.row_ptr, g.col_idx, g.vals, g.n_cols)
         gt = None
-        if any(k == "spmm_t" for k, _ in ops):
+        if any(k.startswith("spmm_t") for k, _ in ops):
             rpt, cit, vt = oracle.transpose(g.row_ptr, g.col_idx, g.vals, g.n_cols)
             gt = synth.Csr(g.n_cols, g.n_rows, rpt, cit, vt)
             t_rp = torch.empty(g.n_cols + 1, dtype=torch.int32, device=dev)
@@ -261,10 +262,13 @@ def large_config_rows(dev, flush, stream, steps, warmup, oracle_frac=0.05):
                 b = sddmm_bytes(g.n_rows, g.nnz, F, 4)
                 del Q, K, S
             else:
-                tr = kind == "spmm_t"
+                # mean aggregation's values are fixed: SpMM^T plans keep them in A^T order;
+                # spmm_t_vpc reads them per call (gathered into A^T order at every call)
+                tr = kind.startswith("spmm_t")
                 X = torch.randn(g.n_rows if tr else g.n_cols, F, device=dev)
                 Y = torch.empty(g.n_cols if tr else g.n_rows, F, device=dev)
-                plan = sga.autosage_plan(A, sga.OP_SPMM_T if tr else sga.OP_SPMM, F, flags=flags)
+                fl = flags | (sga.PLAN_FIXED_VALUES if kind == "spmm_t" else 0)
+                plan = sga.autosage_plan(A, sga.OP_SPMM_T if tr else sga.OP_SPMM, F, flags=fl)
                 ms = timed(lambda: sga.autosage_spmm(A, X, Y, transpose=tr, plan=plan))
                 b = spmm_bytes(g.n_rows, g.nnz, F, 4)
                 del X, Y
@@ -394,7 +398,8 @@ def run_ours(args):
         if kind == "spmm":
             plans[key] = sga.autosage_plan(A, sga.OP_SPMM, F, flags=flags)
         elif kind == "spmm_t":
-            plans[key] = sga.autosage_plan(A, sga.OP_SPMM_T, F, flags=flags)
+            # the step's edge values do not change: the plan keeps them in A^T order
+            plans[key] = sga.autosage_plan(A, sga.OP_SPMM_T, F, flags=flags | sga.PLAN_FIXED_VALUES)
         elif kind == "sddmm":
             plans[key] = sga.autosage_plan(A, sga.OP_SDDMM, F, flags=flags)
         elif kind == "attn_fused":

@@ -101,6 +101,13 @@ typedef struct autosage_plan_s *autosage_plan_t;
 #define AUTOSAGE_PLAN_PROBE 1u     /* refine the estimate with on-device micro-probes */
 #define AUTOSAGE_PLAN_NO_CACHE 2u  /* neither read nor write the persistent cache */
 #define AUTOSAGE_PLAN_VERIFY 4u    /* spot-check each probed candidate against the default */
+/* The edge values given at plan time are fixed for the plan's life (a normalised adjacency
+ * such as mean aggregation, 1/deg): every call must pass the same A->vals array (checked;
+ * AUTOSAGE_ERR_PLAN_MISMATCH otherwise) and must not have changed its contents. SpMM with
+ * A^T then gathers the values into A^T's edge order once, at plan time (and again in
+ * autosage_plan_rebind), instead of at every call. Without this flag every call reads the
+ * values it is passed. */
+#define AUTOSAGE_PLAN_FIXED_VALUES 8u
 
 /* ---------------------------------------------------------------- ops */
 
@@ -209,6 +216,40 @@ autosage_status autosage_csr_attention_unfused_noalloc(const autosage_csr *A, co
                                                        int64_t D, autosage_dtype dt, float scale,
                                                        void *out, void *stream);
 
+/* ---------------------------------------------------------------- row sharding (several GPUs)
+ *
+ * Every op is defined per destination row (Abstract; benchmark page, problem statement: an
+ * output row per destination node from its incoming edges), so contiguous row ranges are
+ * independent units. A multi-GPU job gives each process (one per GPU) a shard: a range of rows
+ * with about equal edge counts. The shard needs the feature rows its edges reference (its
+ * halo), which one exchange step brings to its GPU (e.g. an all-gather of the row blocks the
+ * processes own, then autosage_gather_rows); its outputs are its own rows, so nothing is
+ * reduced afterwards. SpMM with A^T shards the rows of A^T. The partition and halo are
+ * computed on the host once per graph; the ops themselves run unchanged on the shard's CSR. */
+
+/* Cut the n_rows rows of a CSR into `parts` contiguous ranges of about equal nnz. row_ptr is
+ * a HOST array [n_rows + 1]; bounds is a HOST array [parts + 1] that receives the first row of
+ * each part (bounds[0] = 0, bounds[parts] = n_rows; part k is rows [bounds[k], bounds[k+1]),
+ * possibly empty). Returns AUTOSAGE_ERR_INVALID_CSR if row_ptr[0] != 0 or row_ptr decreases. */
+autosage_status autosage_partition_rows(const int32_t *row_ptr, int64_t n_rows, int parts, int64_t *bounds);
+
+/* Halo of the shard of rows [row_begin, row_end) of a HOST CSR (row_ptr, col_idx): the distinct
+ * columns its edges reference, in increasing order, written to halo (HOST, capacity n_cols;
+ * their count to *n_halo), and for each edge p of the shard (p - row_ptr[row_begin] in
+ * [0, shard nnz)) the position of its column in halo, written to local_col (HOST). The shard's
+ * CSR with row_ptr[row_begin..row_end] - row_ptr[row_begin], local_col and n_cols = *n_halo
+ * then addresses a dense matrix of the halo rows only. Columns outside [0, n_cols) return
+ * AUTOSAGE_ERR_INVALID_CSR. */
+autosage_status autosage_shard_halo(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_cols,
+                                    int64_t row_begin, int64_t row_end, int32_t *halo, int64_t *n_halo,
+                                    int32_t *local_col);
+
+/* out[k, :] = X[idx[k], :] for k < n on the GPU (DEVICE pointers; rows of F elements of type
+ * dt, leading dimensions ldx and ldo in elements; each idx[k] must be a row of X). Packs a
+ * shard's halo rows into a dense matrix. Asynchronous on `stream`. */
+autosage_status autosage_gather_rows(const void *X, int64_t ldx, const int32_t *idx, int64_t n, int64_t F,
+                                     autosage_dtype dt, void *out, int64_t ldo, void *stream);
+
 /* ---------------------------------------------------------------- planning */
 
 /* Build a plan for (A, op, F, heads, dt). For attention ops F is the head dimension D.
@@ -238,14 +279,16 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
  * refuses arrays that were overwritten with another graph. The edge values are NOT part
  * of the binding: every call reads A->vals as passed (for SpMM with A^T they are gathered
  * into A^T's edge order on the stream at each call), so new values per layer or step need
- * no new plan. A typed plan is bound to row_ptr, col_idx and edge_type.
+ * no new plan, unless the plan was built with AUTOSAGE_PLAN_FIXED_VALUES (see there).
+ * A typed plan is bound to row_ptr, col_idx and edge_type.
  * A plan's workspace is shared by its calls: calls of one plan that overlap on the GPU
  * (several streams or threads) race on it; serialise them or use one plan per stream. */
 
 /* Rebind a plan to structure arrays that moved (a copy of the same graph in new device
  * memory). Computes the fingerprint of A's structure on the GPU (SYNCHRONISES `stream`)
  * and accepts A only if its sizes and fingerprint equal those of the plan's graph;
- * otherwise returns AUTOSAGE_ERR_PLAN_MISMATCH and leaves the plan unchanged. Typed plans
+ * otherwise returns AUTOSAGE_ERR_PLAN_MISMATCH and leaves the plan unchanged. A plan with
+ * fixed values takes A->vals as its new fixed values. Typed plans
  * return AUTOSAGE_ERR_UNSUPPORTED (their combined index is built from the edge types). */
 autosage_status autosage_plan_rebind(autosage_plan_t plan, const autosage_csr *A, void *stream);
 

@@ -29,7 +29,7 @@ ERR_CACHE_IO, ERR_CACHE_FORMAT, ERR_PROBE, ERR_PLAN_MISMATCH = 5, 6, 7, 8
 F32, BF16 = 0, 1
 OP_SPMM, OP_SPMM_T, OP_SDDMM, OP_ATTN, OP_ATTN_UNFUSED, OP_SOFTMAX, OP_ATTN_BACKWARD = 0, 1, 2, 3, 4, 5, 6
 SCHED_AUTO, SCHED_ROWGROUP, SCHED_SPLIT, SCHED_MERGEPATH, SCHED_BINNED = -1, 0, 1, 2, 3
-PLAN_PROBE, PLAN_NO_CACHE, PLAN_VERIFY = 1, 2, 4
+PLAN_PROBE, PLAN_NO_CACHE, PLAN_VERIFY, PLAN_FIXED_VALUES = 1, 2, 4, 8
 
 EXPORTS = [
     "autosage_spmm", "autosage_sddmm", "autosage_row_softmax", "autosage_csr_attention",
@@ -40,6 +40,7 @@ EXPORTS = [
     "autosage_status_string", "autosage_last_error", "autosage_version",
     "autosage_csr_attention_unfused_noalloc", "autosage_csr_attention_backward",
     "autosage_plan_typed", "autosage_spmm_typed", "autosage_plan_rebind",
+    "autosage_partition_rows", "autosage_shard_halo", "autosage_gather_rows",
 ]
 
 
@@ -89,6 +90,9 @@ def _load():
         "autosage_fingerprint": [CSR, ctypes.POINTER(ctypes.c_uint64), P],
         "autosage_validate_csr": [CSR, P],
         "autosage_csr_transpose": [CSR, P, P, P, P],
+        "autosage_partition_rows": [P, I64, I, P],
+        "autosage_shard_halo": [P, P, I64, I64, I64, P, P, P],
+        "autosage_gather_rows": [P, I64, P, I64, I64, I, P, I64, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -452,6 +456,42 @@ def autosage_csr_transpose(A: CsrMatrix, stream=None):
     vt = None if A.vals is None else torch.empty(max(A.nnz, 1), dtype=torch.float32, device=dev)[:A.nnz]
     _check(_lib.autosage_csr_transpose(A.c, _ptr(rpt), _ptr(cit), _ptr(vt), _stream(stream)))
     return rpt, cit, vt
+
+
+def autosage_partition_rows(row_ptr, parts: int):
+    """Equal-nnz row ranges of a HOST CSR: int64 bounds [parts + 1] (part k = rows bounds[k]..bounds[k+1])."""
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    bounds = np.zeros(int(parts) + 1, dtype=np.int64)
+    _check(_lib.autosage_partition_rows(rp.ctypes.data_as(ctypes.c_void_p), rp.size - 1, int(parts),
+                                        bounds.ctypes.data_as(ctypes.c_void_p)))
+    return bounds
+
+
+def autosage_shard_halo(row_ptr, col_idx, n_cols: int, row_begin: int, row_end: int):
+    """(halo, local_col) of the shard rows [row_begin, row_end) of a HOST CSR: the sorted distinct
+    columns its edges reference, and each edge's column as a position in that list."""
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    halo = np.empty(max(int(n_cols), 1), dtype=np.int32)
+    local = np.empty(max(int(rp[row_end] - rp[row_begin]), 1), dtype=np.int32)
+    nh = ctypes.c_int64()
+    _check(_lib.autosage_shard_halo(rp.ctypes.data_as(ctypes.c_void_p), ci.ctypes.data_as(ctypes.c_void_p),
+                                    int(n_cols), int(row_begin), int(row_end), halo.ctypes.data_as(ctypes.c_void_p),
+                                    ctypes.byref(nh), local.ctypes.data_as(ctypes.c_void_p)))
+    return halo[:nh.value].copy(), local[:int(rp[row_end] - rp[row_begin])].copy()
+
+
+def autosage_gather_rows(X, idx, out=None, stream=None):
+    """out[k] = X[idx[k]] on the GPU (X 2-D float32/bfloat16 with unit column stride, idx int32)."""
+    torch = _torch()
+    if idx.dtype != torch.int32 or not idx.is_contiguous():
+        raise TypeError("idx must be a contiguous int32 tensor")
+    F = int(X.shape[1])
+    if out is None:
+        out = torch.empty((int(idx.numel()), F), dtype=X.dtype, device=X.device)
+    _check(_lib.autosage_gather_rows(_ptr(X), _ld(X), _ptr(idx), int(idx.numel()), F, _dt(X), _ptr(out), _ld(out),
+                                     _stream(stream)))
+    return out
 
 
 def autosage_cache_load(path: str):

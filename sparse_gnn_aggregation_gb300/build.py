@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libautosage.so")
-SOURCES = ["spmm.cu", "sddmm.cu", "softmax.cu", "attention.cu", "graph.cu", "runtime.cu", "noalloc.cu", "backward.cu"]
+SOURCES = ["spmm.cu", "sddmm.cu", "softmax.cu", "attention.cu", "graph.cu", "runtime.cu", "noalloc.cu", "backward.cu",
+           "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

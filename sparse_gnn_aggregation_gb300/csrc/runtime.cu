@@ -260,6 +260,10 @@ struct autosage_plan_s {
   // a_fp is the fingerprint of A's structure (autosage_plan_rebind checks it).
   autosage_csr a0{};
   uint64_t a_fp = 0;
+  // AUTOSAGE_PLAN_FIXED_VALUES: the edge values are part of the plan (SPMM_T
+  // keeps them in A^T order in t_vals); calls must pass this value array
+  bool fixed_vals = false;
+  const float *fixed_vals_ptr = nullptr;
   // the CSR the plan's workspace was built over (A, or A^T for SPMM_T)
   int64_t k_rows = 0;
   const int32_t *k_row_ptr = nullptr;
@@ -506,7 +510,20 @@ cudaError_t walk_for(const autosage_plan_s *P, autosage_op op, const autosage_cs
   w = Walk{P->k_rows, P->k_row_ptr, P->k_col_idx, nullptr};
   if (!A->vals || A->nnz == 0) return cudaSuccess;
   w.vals = P->t_vals.as<float>();
+  if (P->fixed_vals) return cudaSuccess;  // gathered once, when the values were fixed
   return launch_gather_vals(A->nnz, P->t_perm.as<int32_t>(), A->vals, P->t_vals.as<float>(), s);
+}
+
+// Fix the plan's edge values to A->vals (FIXED_VALUES plans): SPMM_T gathers
+// them into A^T's edge order once, here, instead of at every call.
+autosage_status fix_values(autosage_plan_s *P, const autosage_csr *A, cudaStream_t s) {
+  P->fixed_vals = true;
+  P->fixed_vals_ptr = A->vals;
+  if (P->op == AUTOSAGE_OP_SPMM_T && A->vals && A->nnz > 0) {
+    CUDA_TRY(launch_gather_vals(A->nnz, P->t_perm.as<int32_t>(), A->vals, P->t_vals.as<float>(), s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+  }
+  return AUTOSAGE_OK;
 }
 
 // Run `op` over the call's A with plan P's schedule (plan-free runs use a
@@ -901,6 +918,10 @@ bool cand_geom(const autosage_plan_s *P, int G, int E, Geom &g) {
   g = Geom{};
   g.dt = P->dt; g.H = sh.H; g.D = sh.D; g.VW = vb / s; g.nfrag = (int)nfrag; g.G = G; g.E = E;
   g.NV = pow2ceil((nfrag + G - 1) / G);
+  // SpMM runs rows wider than 16 fragments per lane as column tiles of 16
+  // fragments per lane, one launch after another: each launch is a candidate
+  // of that geometry
+  if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && g.NV > 16) g.NV = 16;
   return g.NV <= sh.nv_max;
 }
 
@@ -1137,6 +1158,10 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
   autosage_plan_s *P = nullptr;
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
+  if ((flags & AUTOSAGE_PLAN_FIXED_VALUES) && (st = fix_values(P, A, s)) != AUTOSAGE_OK) {
+    delete P;
+    return st;
+  }
   if (op == AUTOSAGE_OP_ATTN_BACKWARD) {  // fixed schedule (no probes)
     st = build_backward_plan(P, default_backward_sched(), s);
     if (st != AUTOSAGE_OK) {
@@ -1350,9 +1375,10 @@ autosage_status autosage_plan_destroy(autosage_plan_t plan) {
 autosage_status autosage_plan_describe(autosage_plan_t P, char *buf, size_t len) {
   if (!P || !buf || len == 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad describe arguments");
   snprintf(buf, len, "op=%d sched=%s G=%d E=%d split=%d chunks=%d long_rows=%d mp_warps=%" PRId64
-           " probe_ms=%.4f est_ms=%.4f cache=%d per_edge=%d",
+           " probe_ms=%.4f est_ms=%.4f cache=%d per_edge=%d fixed_vals=%d",
            (int)P->op, sched_name(P->sched.kind), P->sched.G, P->sched.E, P->sched.split, P->cl.n_chunks,
-           P->cl.n_long, P->mp_warps, P->probe_ms, P->est_ms, P->from_cache ? 1 : 0, P->sched.pe);
+           P->cl.n_long, P->mp_warps, P->probe_ms, P->est_ms, P->from_cache ? 1 : 0, P->sched.pe,
+           P->fixed_vals ? 1 : 0);
   return AUTOSAGE_OK;
 }
 
@@ -1379,6 +1405,7 @@ autosage_status autosage_plan_rebind(autosage_plan_t P, const autosage_csr *A, v
   uint64_t fp = 0;
   if ((st = autosage_fingerprint(A, &fp, stream)) != AUTOSAGE_OK) return st;
   if (fp != P->a_fp) return fail(AUTOSAGE_ERR_PLAN_MISMATCH, "A has another structure than the plan's graph");
+  if (P->fixed_vals && (st = fix_values(P, A, as_stream(stream))) != AUTOSAGE_OK) return st;
   P->a0 = *A;
   if (P->op != AUTOSAGE_OP_SPMM_T) {
     P->k_row_ptr = A->row_ptr;
@@ -1411,6 +1438,10 @@ static autosage_status plan_matches(const autosage_plan_s *P, const autosage_csr
     return fail(AUTOSAGE_ERR_PLAN_MISMATCH,
                 "row_ptr / col_idx are not the arrays the plan was built for (after moving or copying the "
                 "structure, call autosage_plan_rebind)");
+  if (P->fixed_vals && A->vals != P->fixed_vals_ptr)
+    return fail(AUTOSAGE_ERR_PLAN_MISMATCH,
+                "the plan holds fixed edge values (AUTOSAGE_PLAN_FIXED_VALUES) of another array; pass that "
+                "array, or call autosage_plan_rebind with the new one");
   if (check_mode()) {
     uint64_t fp = 0;
     autosage_status st = autosage_fingerprint(A, &fp, stream);

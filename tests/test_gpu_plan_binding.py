@@ -189,3 +189,30 @@ def test_typed_plan_reads_the_calls_values_and_checks_its_arrays(graphs):
     with pytest.raises(sga.AutosageError) as e:
         plan.rebind(copy_of(A2))
     assert e.value.status == sga.ERR_UNSUPPORTED
+
+
+def test_fixed_values_plan_keeps_its_values_and_checks_the_array(graphs):
+    # AUTOSAGE_PLAN_FIXED_VALUES: SpMM with A^T gathers the values into A^T's
+    # edge order once; a call must pass the same value array, and rebinding
+    # takes the new array's values
+    g, v2, _ = graphs
+    F = 8
+    A = sga.CsrMatrix.from_numpy(g.row_ptr, g.col_idx, g.vals, g.n_cols)
+    G = synth.normal(g.n_rows, F, 8, synth.STREAM_G)
+    plan = sga.autosage_plan(A, sga.OP_SPMM_T, F, flags=sga.PLAN_NO_CACHE | sga.PLAN_FIXED_VALUES)
+    assert "fixed_vals=1" in plan.describe()
+    want1 = oracle.spmm_t(g.row_ptr, g.col_idx, g.vals, G, g.n_cols)
+    for _ in range(2):
+        assert_close(to_np(sga.autosage_spmm(A, dev(G), transpose=True, plan=plan)), want1, TOL_F32, "fixed values")
+    A2 = sga.CsrMatrix(A.row_ptr, A.col_idx, dev(v2), A.n_cols)
+    with pytest.raises(sga.AutosageError) as e:
+        sga.autosage_spmm(A2, dev(G), transpose=True, plan=plan)
+    assert e.value.status == sga.ERR_PLAN_MISMATCH
+    plan.rebind(A2)
+    want2 = oracle.spmm_t(g.row_ptr, g.col_idx, v2, G, g.n_cols)
+    assert_close(to_np(sga.autosage_spmm(A2, dev(G), transpose=True, plan=plan)), want2, TOL_F32, "refixed values")
+    # forward ops read the values from the call's array (the same array here)
+    fplan = sga.autosage_plan(A2, sga.OP_SPMM, F, flags=sga.PLAN_NO_CACHE | sga.PLAN_FIXED_VALUES)
+    X = synth.normal(g.n_cols, F, 8, synth.STREAM_X)
+    assert_close(to_np(sga.autosage_spmm(A2, dev(X), plan=fplan)), oracle.spmm(g.row_ptr, g.col_idx, v2, X),
+                 TOL_F32, "forward, fixed values")
