@@ -437,8 +437,12 @@ def run_ours(args):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
+                # an NVTX range per timed operation: a profiler can name the
+                # operation's kernel launches by its key
+                torch.cuda.nvtx.range_push(key)
             run(key, kind, gname, F, feats[key], outs[key])
             if timed:
+                torch.cuda.nvtx.range_pop()
                 e1.record(stream)
                 ev[key].append((e0, e1))
 
