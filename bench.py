@@ -354,7 +354,7 @@ def aggregate_ranks(step_ms, step_bytes, world, device="cpu"):
         t = torch.tensor([float(step_ms)], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         step_ms = float(t.item())
-    return step_ms, step_bytes * world / (step_ms * 1e-3) / 1e9
+    return step_ms, (step_bytes * world / (step_ms * 1e-3) / 1e9 if step_ms > 0 else 0.0)
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -561,10 +561,10 @@ def run_ours(args):
 
     # dominant operation: the largest share of the step
     # (one main kernel per launch: the unfused pipeline is three kernels, so it is not a candidate)
-    dom_key = max((k for k in per_op if not k.startswith("attn_unfused")), key=lambda k: per_op[k]["ms"])
-    dom = per_op[dom_key]
+    cands = [k for k in per_op if not k.startswith("attn_unfused")]
+    dom_key = max(cands, key=lambda k: per_op[k]["ms"]) if cands else None
     peak, peak_src = measured_peak()
-    achieved = dom["GBps"]
+    achieved = per_op[dom_key]["GBps"] if dom_key else None
 
     # end to end through the public API with host buffers: H2D inputs, op, D2H output
     e2e = None
@@ -647,11 +647,12 @@ def run_ours(args):
         "data": "synthetic",
         "config": workload_config(graphs, world),
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
-        "nnzF_per_s": tot_nnzF * world / (step_ms * 1e-3),
-        "edges_per_s": sum(graphs[g].nnz for _, _, g, _ in ops) * world / (step_ms * 1e-3),
+        "nnzF_per_s": tot_nnzF * world / max(step_ms * 1e-3, 1e-12),
+        "edges_per_s": sum(graphs[g].nnz for _, _, g, _ in ops) * world / max(step_ms * 1e-3, 1e-12),
         "roofline": {"bound": "hbm", "kernel": dom_key, "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_for(dom_key)},
+                     "unit": "GB/s", "frac": round(achieved / peak, 4) if dom_key else None,
+                     "traffic": traffic_for(dom_key) if dom_key else None},
         "clocks": clock_info,
         "gpu_launches": n_launch,
         "plan_seconds": round(plan_s, 2),
