@@ -70,8 +70,12 @@ typedef enum {
                                     partial results are combined in a fixed order */
   AUTOSAGE_SCHED_MERGEPATH = 2,  /* equal (rows + edges) share per warp along the merge path,
                                     carry-out of rows cut at warp boundaries, fixed-order fix-up */
-  AUTOSAGE_SCHED_BINNED = 3      /* SPLIT, with rows taken in order of degree bucket (longest
+  AUTOSAGE_SCHED_BINNED = 3,     /* SPLIT, with rows taken in order of degree bucket (longest
                                     first) so the lane groups of a warp get rows of similar length */
+  AUTOSAGE_SCHED_HYBRID = 4      /* SpMM only: BINNED for rows of 8 or more edges, and the rows of
+                                    1..7 edges kept in an ELL slab (8 column slots per row,
+                                    column-major) that one lane group per row reads with
+                                    coalesced loads (composable formats: ELL + CSR) */
 } autosage_sched_kind;
 
 typedef struct {

@@ -28,7 +28,7 @@ OK, ERR_INVALID_ARG, ERR_INVALID_CSR, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
 ERR_CACHE_IO, ERR_CACHE_FORMAT, ERR_PROBE, ERR_PLAN_MISMATCH = 5, 6, 7, 8
 F32, BF16 = 0, 1
 OP_SPMM, OP_SPMM_T, OP_SDDMM, OP_ATTN, OP_ATTN_UNFUSED, OP_SOFTMAX, OP_ATTN_BACKWARD = 0, 1, 2, 3, 4, 5, 6
-SCHED_AUTO, SCHED_ROWGROUP, SCHED_SPLIT, SCHED_MERGEPATH, SCHED_BINNED = -1, 0, 1, 2, 3
+SCHED_AUTO, SCHED_ROWGROUP, SCHED_SPLIT, SCHED_MERGEPATH, SCHED_BINNED, SCHED_HYBRID = -1, 0, 1, 2, 3, 4
 PLAN_PROBE, PLAN_NO_CACHE, PLAN_VERIFY, PLAN_FIXED_VALUES = 1, 2, 4, 8
 
 EXPORTS = [

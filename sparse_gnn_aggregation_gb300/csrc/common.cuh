@@ -244,6 +244,7 @@ constexpr int kMaxRuns = 34;  // chunks, 32 degree buckets, rows longer than spl
 struct RunTable {
   int n = 0;
   int64_t item0[kMaxRuns + 1];  // first item of segment s; item0[n] = items
+  int64_t item1[kMaxRuns];      // one past the last item of segment s
   int block0[kMaxRuns + 1];     // first block of segment s; block0[n] = grid
   int run[kMaxRuns];            // items per block in segment s
 };
@@ -260,6 +261,9 @@ struct ChunkList {
   // degree-binned order: rows of bucket k (k = 0: the longest) start at
   // position bucket_start[k] of row_order; bucket_start[32] = n_rows
   int32_t bucket_start[33] = {};
+  // buckets [ell_from, ell_to) are handled by an ELL slab (hybrid schedule):
+  // the row launch skips their items
+  int ell_from = 32, ell_to = 32;
   RunTable runs;
 };
 
@@ -315,7 +319,7 @@ struct ItemQueue {
       while (sg + 1 < T.n && (int)blockIdx.x >= T.block0[sg + 1]) ++sg;
       base = T.item0[sg] + (int64_t)((int)blockIdx.x - T.block0[sg]) * T.run[sg];
       const int64_t stop = base + T.run[sg];
-      end = stop < T.item0[sg + 1] ? stop : T.item0[sg + 1];
+      end = stop < T.item1[sg] ? stop : T.item1[sg];
     } else {
       base = (int64_t)blockIdx.x * ipb;
       const int64_t n_items = n_rows + cl.n_chunks;
@@ -359,6 +363,7 @@ inline Deal deal_items(const ChunkList &cl, int64_t n_rows, int GE, int G) {
   auto add = [&](int64_t count, int run) {
     if (count <= 0) return;
     T.item0[T.n] = item;
+    T.item1[T.n] = item + count;
     T.block0[T.n] = static_cast<int>(block);
     T.run[T.n] = run;
     item += count;
@@ -373,6 +378,10 @@ inline Deal deal_items(const ChunkList &cl, int64_t n_rows, int GE, int G) {
     // degree buckets, longest first: bucket k holds degrees below 2^(31 - k)
     // (the last bucket: rows longer than split, which are inactive items)
     for (int k = 0; k < 32; ++k) {
+      if (k >= cl.ell_from && k < cl.ell_to) {  // rows of the ELL slab: not items of this launch
+        item += (int64_t)cl.bucket_start[k + 1] - cl.bucket_start[k];
+        continue;
+      }
       const int bits = 31 - k;
       int pg = k == 31 || bits >= 10 ? 1 : 512 >> bits;
       if (k == 31) pg = max_per_group;

@@ -324,6 +324,21 @@ __global__ void gather_vals_kernel(int64_t nnz, const int32_t *__restrict__ perm
     __stcs(out + k, __ldg(vals + __ldcs(perm + k)));
 }
 
+// ELL slab of the n rows at positions [pos0, pos0 + n) of a degree-binned
+// order (each of degree <= W): col[j * n + e] = column of edge j of row
+// order[pos0 + e], -1 past the row's end (column-major: lanes that take
+// consecutive rows read consecutive words); start[e] = the row's first edge.
+__global__ void ell_build_kernel(int64_t n, int W, const int32_t *__restrict__ order, int64_t pos0,
+                                 const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
+                                 int32_t *__restrict__ col, int32_t *__restrict__ start) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  const int32_t r = order[pos0 + e];
+  const int b = row_ptr[r], d = row_ptr[r + 1] - b;
+  start[e] = b;
+  for (int j = 0; j < W; ++j) col[(int64_t)j * n + e] = j < d ? col_idx[b + j] : -1;
+}
+
 __global__ void degree_key_kernel(int64_t n_rows, const int32_t *__restrict__ row_ptr, int split,
                                   int32_t *__restrict__ keys, int32_t *__restrict__ vals) {
   const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -565,6 +580,13 @@ cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, i
     if (*bufs[i]) cudaFreeAsync(*bufs[i], s);
   if (scan_tmp) cudaFreeAsync(scan_tmp, s);
   return err;
+}
+
+cudaError_t build_ell(int64_t n, int W, const int32_t *order, int64_t pos0, const int32_t *row_ptr,
+                      const int32_t *col_idx, int32_t *col, int32_t *start, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  ell_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(n, W, order, pos0, row_ptr, col_idx, col, start);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gather_vals(int64_t nnz, const int32_t *perm, const float *vals, float *out, cudaStream_t s) {

@@ -117,6 +117,17 @@ cudaError_t launch_invert_perm(int64_t n, const int32_t *perm, int32_t *inv, cud
 // than split); bucket_start[32] = n_rows. Synchronises s when given.
 cudaError_t build_row_order(int64_t n_rows, const int32_t *row_ptr, int split, int32_t *order,
                             int32_t *bucket_start, cudaStream_t s);
+// ELL slab (hybrid schedule) of the n rows at positions [pos0, pos0 + n) of a
+// degree-binned order, each of degree <= W: col [W * n] column-major (-1
+// pads), start [n] the first edge of each row.
+cudaError_t build_ell(int64_t n, int W, const int32_t *order, int64_t pos0, const int32_t *row_ptr,
+                      const int32_t *col_idx, int32_t *col, int32_t *start, cudaStream_t s);
+// SpMM over an ELL slab (hybrid schedule): rows order[pos0 + e] for e < n,
+// edge j of row e has column ell_col[j * n + e] (or -1) and value
+// vals[ell_start[e] + j] (vals may be null: 1). Output rows of Y overwritten.
+cudaError_t launch_spmm_ell(const Geom &g, int64_t n, const int32_t *rows, const int32_t *ell_col,
+                            const int32_t *ell_start, const float *vals, const void *X, int64_t ldx, void *Y,
+                            int64_t ldy, cudaStream_t s);
 // out[k] = vals[perm[k]] for k < nnz (edge values carried into A^T's edge order).
 cudaError_t launch_gather_vals(int64_t nnz, const int32_t *perm, const float *vals, float *out, cudaStream_t s);
 // combined[p] = edge_type[p] * n_cols + col_idx[p]; *err (device) gets 1 for a type out of range.

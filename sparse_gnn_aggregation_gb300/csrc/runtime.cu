@@ -235,6 +235,13 @@ autosage_status gpu_row_stats(int64_t n_rows, const int32_t *row_ptr, int64_t th
 
 // ---------------------------------------------------------------- plan
 
+// Hybrid schedule: rows of 1..kEllMaxDegree edges (the degree buckets from
+// key kEllFirstKey of the binned order on) are kept in an ELL slab of
+// kEllSlots columns; every other row runs as in the binned schedule.
+constexpr int kEllSlots = 8;
+constexpr int kEllMaxDegree = 7;
+constexpr int kEllFirstKey = 28;  // bit length 3: degrees 4..7
+
 struct Sched {
   int kind = AUTOSAGE_SCHED_ROWGROUP;
   int G = 0, E = 0, split = 0;
@@ -272,6 +279,10 @@ struct autosage_plan_s {
   DevBuf t_row_ptr, t_col_idx, t_vals;
   // split workspace
   DevBuf long_rows, long_ptr, chunk_row, chunk_begin, partial, ml, row_ml, row_order;
+  // hybrid schedule: the ELL slab of the short rows (positions [ell_pos0,
+  // ell_pos0 + n_ell) of row_order)
+  DevBuf ell_col, ell_start;
+  int64_t n_ell = 0, ell_pos0 = 0;
   ChunkList cl;
   // merge-path workspace
   DevBuf mp_part, mp_carry_val, mp_carry_row, mp_head_val;
@@ -293,7 +304,7 @@ struct autosage_plan_s {
     for (DevBuf *b : {&t_row_ptr, &t_col_idx, &t_vals, &long_rows, &long_ptr, &chunk_row,
                       &chunk_begin, &partial, &ml, &row_ml, &row_order, &mp_part, &mp_carry_val,
                       &mp_carry_row, &mp_head_val, &scores, &t_perm, &t_inv, &grad_dw, &grad_wt, &grad_dst,
-                      &typed_idx})
+                      &typed_idx, &ell_col, &ell_start})
       b->release();
     delete tplan;
   }
@@ -327,6 +338,7 @@ const char *sched_name(int kind) {
     case AUTOSAGE_SCHED_SPLIT: return "split";
     case AUTOSAGE_SCHED_MERGEPATH: return "mergepath";
     case AUTOSAGE_SCHED_BINNED: return "binned";
+    case AUTOSAGE_SCHED_HYBRID: return "hybrid";
   }
   return "?";
 }
@@ -429,9 +441,10 @@ autosage_status build_mergepath(autosage_plan_s *P, int items, int64_t width, cu
 autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
   for (DevBuf *b : {&P->long_rows, &P->long_ptr, &P->chunk_row, &P->chunk_begin, &P->partial,
                     &P->ml, &P->row_ml, &P->row_order, &P->mp_part, &P->mp_carry_val, &P->mp_carry_row,
-                    &P->mp_head_val})
+                    &P->mp_head_val, &P->ell_col, &P->ell_start})
     b->release();
   P->cl = ChunkList{};
+  P->n_ell = 0;
   P->mp_warps = 0;
   autosage_status st = AUTOSAGE_OK;
   if (P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T || P->op == AUTOSAGE_OP_ATTN_BACKWARD) {
@@ -444,18 +457,35 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
     // longest run of edges one lane sums serially (edge lanes taken as 1 when automatic)
     const int64_t lanes_e = P->sched.E > 0 ? P->sched.E : 1;
     int64_t run = P->maxdeg;
-    if (P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED)
+    if (P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED ||
+        P->sched.kind == AUTOSAGE_SCHED_HYBRID)
       run = std::min<int64_t>(run, P->sched.split);
     if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) run = std::min<int64_t>(run, P->sched.split);
     P->comp = run / lanes_e > 512;
   }
-  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED) {
+  const bool hybrid = P->sched.kind == AUTOSAGE_SCHED_HYBRID;
+  if (hybrid && P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)
+    return fail(AUTOSAGE_ERR_UNSUPPORTED, "hybrid (ELL + CSR) schedule is SpMM only");
+  if (hybrid && P->sched.split < kEllMaxDegree)
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "hybrid schedule needs a chunk length of at least %d", kEllMaxDegree);
+  if (P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED || hybrid) {
     st = build_split(P, P->sched.split, s);
-    if (st == AUTOSAGE_OK && P->sched.kind == AUTOSAGE_SCHED_BINNED && P->k_rows > 0) {
+    if (st == AUTOSAGE_OK && P->sched.kind != AUTOSAGE_SCHED_SPLIT && P->k_rows > 0) {
       CUDA_TRY(P->row_order.alloc(sizeof(int32_t) * (size_t)P->k_rows));
       CUDA_TRY(build_row_order(P->k_rows, P->k_row_ptr, P->sched.split, P->row_order.as<int32_t>(),
                                P->cl.bucket_start, s));
       P->cl.row_order = P->row_order.as<int32_t>();
+    }
+    if (st == AUTOSAGE_OK && hybrid && P->k_rows > 0) {
+      // the degree buckets of 1..7 edges (keys 28, 29, 30 of the binned order) go to an ELL slab
+      P->cl.ell_from = kEllFirstKey;
+      P->cl.ell_to = 31;
+      P->ell_pos0 = P->cl.bucket_start[kEllFirstKey];
+      P->n_ell = (int64_t)P->cl.bucket_start[31] - P->ell_pos0;
+      CUDA_TRY(P->ell_col.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(P->n_ell * kEllSlots, 1)));
+      CUDA_TRY(P->ell_start.alloc(sizeof(int32_t) * (size_t)std::max<int64_t>(P->n_ell, 1)));
+      CUDA_TRY(build_ell(P->n_ell, kEllSlots, P->row_order.as<int32_t>(), P->ell_pos0, P->k_row_ptr, P->k_col_idx,
+                         P->ell_col.as<int32_t>(), P->ell_start.as<int32_t>(), s));
     }
   } else if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
     if (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)
@@ -563,6 +593,9 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
         } else {
           e = launch_spmm(gt, wk.rows, wk.row_ptr, wk.col_idx, wk.vals, x, a.ldx, y, a.ldy, cl,
                           P->partial.as<float>(), s);
+          if (e == cudaSuccess && P->n_ell > 0)
+            e = launch_spmm_ell(gt, P->n_ell, P->row_order.as<int32_t>() + P->ell_pos0, P->ell_col.as<int32_t>(),
+                                P->ell_start.as<int32_t>(), wk.vals, x, a.ldx, y, a.ldy, s);
         }
       }
       break;
@@ -701,7 +734,8 @@ double estimate(const DeviceInfo &dev, const RowStats &st, autosage_op op, DType
   const double groups = (double)std::max(1, dev.sms) * 48.0 * (32.0 / lanes_per_item);
   const double lat = 1.2e-6;  // one dependent gather round trip
   double steps = 0, longest = 0;
-  int64_t split = (sc.kind == AUTOSAGE_SCHED_SPLIT || sc.kind == AUTOSAGE_SCHED_BINNED) ? sc.split : 0;
+  int64_t split = (sc.kind == AUTOSAGE_SCHED_SPLIT || sc.kind == AUTOSAGE_SCHED_BINNED ||
+                   sc.kind == AUTOSAGE_SCHED_HYBRID) ? sc.split : 0;
   for (int b = 0; b < 32; ++b) {
     const double cnt = (double)st.ints[8 + b];
     if (cnt == 0) continue;
@@ -729,7 +763,8 @@ double estimate(const DeviceInfo &dev, const RowStats &st, autosage_op op, DType
   const double t_lat = steps * lat / par;
   const double t_tail = longest * lat;
   double launches = 1;
-  if ((sc.kind == AUTOSAGE_SCHED_SPLIT || sc.kind == AUTOSAGE_SCHED_BINNED) && st.ints[6] > 0)
+  if ((sc.kind == AUTOSAGE_SCHED_SPLIT || sc.kind == AUTOSAGE_SCHED_BINNED || sc.kind == AUTOSAGE_SCHED_HYBRID) &&
+      st.ints[6] > 0)
     launches += (op == AUTOSAGE_OP_SOFTMAX ? 3 : 1);
   if (sc.kind == AUTOSAGE_SCHED_MERGEPATH) launches += 1;
   if (op == AUTOSAGE_OP_ATTN_UNFUSED) launches += 2;
@@ -959,6 +994,13 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
         const int split = maxd > 128 ? 128 : (int)std::max<int64_t>(maxd, 1);
         Sched bn{AUTOSAGE_SCHED_BINNED, G, E, split};
         out.push_back({bn, estimate(dev, st, P->op, P->dt, P->F, sh.H, bn, g) * 0.97});
+        // SpMM: the short rows (1..7 edges, degree buckets 1..3) in an ELL slab, when
+        // they are at least a tenth of the rows and a row takes few lanes (small width)
+        const int64_t short_rows = st.ints[9] + st.ints[10] + st.ints[11];
+        if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && G <= 8 && 10 * short_rows >= st.ints[0]) {
+          Sched hy{AUTOSAGE_SCHED_HYBRID, G, E, std::max(split, kEllMaxDegree + 1)};
+          out.push_back({hy, estimate(dev, st, P->op, P->dt, P->F, sh.H, hy, g) * 0.97});
+        }
       }
       if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && G * E == 32) {
         for (int items : {256, 1024}) {
@@ -1017,6 +1059,8 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
       if (x.split < 16 || x.split >= maxd) return;
     } else if (x.kind == AUTOSAGE_SCHED_BINNED) {
       if (softmax || x.split < 16) return;
+    } else if (x.kind == AUTOSAGE_SCHED_HYBRID) {
+      if ((P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T) || x.split < 16) return;
     } else {
       x.split = 0;
     }
@@ -1036,6 +1080,8 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
     for (int s2 : {b.split / 4, b.split * 4}) add(Sched{b.kind, G, E, s2, b.pe});
   if (b.kind == AUTOSAGE_SCHED_SPLIT) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe});
   if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_SPLIT, G, E, b.split, b.pe});
+  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_HYBRID, G, E, b.split, b.pe});
+  if (b.kind == AUTOSAGE_SCHED_HYBRID) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe});
   if (b.kind == AUTOSAGE_SCHED_ROWGROUP && maxd > 128) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, 128, b.pe});
   if (P->op == AUTOSAGE_OP_SDDMM) add(Sched{b.kind, G, E, b.split, 1 - b.pe});
   return out;
@@ -1117,7 +1163,7 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
   if (!out) return fail(AUTOSAGE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!sched) return fail(AUTOSAGE_ERR_INVALID_ARG, "sched is NULL");
-  if (sched->kind < AUTOSAGE_SCHED_ROWGROUP || sched->kind > AUTOSAGE_SCHED_BINNED)
+  if (sched->kind < AUTOSAGE_SCHED_ROWGROUP || sched->kind > AUTOSAGE_SCHED_HYBRID)
     return fail(AUTOSAGE_ERR_INVALID_ARG, "bad schedule kind");
   if ((sched->lanes_f && !is_pow2(sched->lanes_f)) || (sched->lanes_e && !is_pow2(sched->lanes_e)) ||
       sched->lanes_f > 32 || sched->lanes_e > 32 || sched->lanes_f * std::max(1, sched->lanes_e) > 32)
@@ -1128,7 +1174,8 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
   P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split, sched->per_edge ? 1 : 0};
-  if ((P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED) && P->sched.split == 0)
+  if ((P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED ||
+       P->sched.kind == AUTOSAGE_SCHED_HYBRID) && P->sched.split == 0)
     P->sched.split = 1024;
   if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH && P->sched.split == 0) P->sched.split = 512;
   if (P->sched.kind == AUTOSAGE_SCHED_ROWGROUP) P->sched.split = 0;
@@ -1233,7 +1280,8 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
     };
     // the estimate ranks lane counts poorly, so every (family, feature lanes)
     // pair sends its best candidate to the probes
-    for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH, AUTOSAGE_SCHED_BINNED}) {
+    for (int kind : {AUTOSAGE_SCHED_ROWGROUP, AUTOSAGE_SCHED_SPLIT, AUTOSAGE_SCHED_MERGEPATH, AUTOSAGE_SCHED_BINNED,
+                     AUTOSAGE_SCHED_HYBRID}) {
       std::vector<int> seen_g;
       for (const Candidate &c : cands) {
         const int gk = c.sc.G * 2 + c.sc.pe;
@@ -1853,6 +1901,7 @@ autosage_status autosage_cache_load(const char *path) {
     else if (kind == "split") e.sched.kind = AUTOSAGE_SCHED_SPLIT;
     else if (kind == "mergepath") e.sched.kind = AUTOSAGE_SCHED_MERGEPATH;
     else if (kind == "binned") e.sched.kind = AUTOSAGE_SCHED_BINNED;
+    else if (kind == "hybrid") e.sched.kind = AUTOSAGE_SCHED_HYBRID;
     else {
       ++bad;
       continue;

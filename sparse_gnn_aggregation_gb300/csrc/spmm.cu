@@ -320,6 +320,79 @@ __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
   }
 }
 
+// ---------------------------------------------------------------- ELL slab (hybrid schedule)
+
+// Width of the ELL slab: the rows of degree 1..7 (three degree buckets).
+constexpr int kEllWidth = 8;
+
+// G feature lanes per row, one row per lane group: the row's kEllWidth column
+// slots are loaded at once (column-major, so consecutive rows' lanes read
+// consecutive words); the gathers of SU real slots are in flight together
+// (SU * NV <= 8 fragments per lane), and the row's sum is taken in slot order.
+template <typename T, int VW, int NV>
+__global__ void __launch_bounds__(kBlock) spmm_ell_kernel(int64_t n, const int32_t *__restrict__ rows,
+                                                          const int32_t *__restrict__ ell_col,
+                                                          const int32_t *__restrict__ ell_start,
+                                                          const float *__restrict__ vals, const T *__restrict__ X,
+                                                          int64_t ldx, T *__restrict__ Y, int64_t ldy, int nfrag,
+                                                          int G) {
+  constexpr int SU = NV >= 8 ? 1 : 8 / NV;
+  const int64_t t = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+  const int64_t e = t / G;
+  const int g = (int)(t - e * G);
+  if (e >= n) return;  // no shuffles below: lanes may leave on their own
+  int c[kEllWidth];
+#pragma unroll
+  for (int j = 0; j < kEllWidth; ++j) c[j] = ld_stream_i32(ell_col + (int64_t)j * n + e);
+  const int st = ld_stream_i32(ell_start + e);
+  float acc[NV][VW];
+  zero(acc);
+#pragma unroll
+  for (int j0 = 0; j0 < kEllWidth; j0 += SU) {
+    float w[SU];
+    Frag<T, VW> f[SU][NV];
+#pragma unroll
+    for (int j = 0; j < SU; ++j) {
+      w[j] = (vals && c[j0 + j] >= 0) ? __ldg(vals + st + j0 + j) : 1.f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (c[j0 + j] >= 0 && g + k * G < nfrag) f[j][k].load(X + (int64_t)c[j0 + j] * ldx + (int64_t)(g + k * G) * VW);
+    }
+#pragma unroll
+    for (int j = 0; j < SU; ++j)
+      if (c[j0 + j] >= 0)
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (g + k * G < nfrag)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) acc[k][v] = fmaf(w[j], f[j][k].get(v), acc[k][v]);
+  }
+  T *y = Y + (int64_t)ld_stream_i32(rows + e) * ldy;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (g + k * G < nfrag) store_frag<T, VW>(y + (int64_t)(g + k * G) * VW, acc[k]);
+}
+
+template <typename T, int VW>
+cudaError_t spmm_ell_vw(const Geom &g, int64_t n, const int32_t *rows, const int32_t *ell_col,
+                        const int32_t *ell_start, const float *vals, const T *X, int64_t ldx, T *Y, int64_t ldy,
+                        cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((n * g.G + kBlock - 1) / kBlock);
+#define AUTOSAGE_ELL(NVV) \
+  spmm_ell_kernel<T, VW, NVV><<<grid, kBlock, 0, s>>>(n, rows, ell_col, ell_start, vals, X, ldx, Y, ldy, g.nfrag, g.G)
+  switch (g.NV) {
+    case 1: AUTOSAGE_ELL(1); break;
+    case 2: AUTOSAGE_ELL(2); break;
+    case 4: AUTOSAGE_ELL(4); break;
+    case 8: AUTOSAGE_ELL(8); break;
+    case 16: AUTOSAGE_ELL(16); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef AUTOSAGE_ELL
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- dispatch
 
 template <typename T, int VW>
@@ -411,6 +484,30 @@ cudaError_t launch_spmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
       case 4: return spmm_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
       case 2: return spmm_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
       case 1: return spmm_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, cl, partial, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_spmm_ell(const Geom &g, int64_t n, const int32_t *rows, const int32_t *ell_col,
+                            const int32_t *ell_start, const float *vals, const void *X, int64_t ldx, void *Y,
+                            int64_t ldy, cudaStream_t s) {
+  if (g.dt == DType::F32) {
+    auto x = static_cast<const float *>(X);
+    auto y = static_cast<float *>(Y);
+    switch (g.VW) {
+      case 4: return spmm_ell_vw<float, 4>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
+      case 2: return spmm_ell_vw<float, 2>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
+      case 1: return spmm_ell_vw<float, 1>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
+    }
+  } else {
+    auto x = static_cast<const __nv_bfloat16 *>(X);
+    auto y = static_cast<__nv_bfloat16 *>(Y);
+    switch (g.VW) {
+      case 8: return spmm_ell_vw<__nv_bfloat16, 8>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
+      case 4: return spmm_ell_vw<__nv_bfloat16, 4>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
+      case 2: return spmm_ell_vw<__nv_bfloat16, 2>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
+      case 1: return spmm_ell_vw<__nv_bfloat16, 1>(g, n, rows, ell_col, ell_start, vals, x, ldx, y, ldy, s);
     }
   }
   return cudaErrorInvalidValue;

@@ -44,6 +44,20 @@ def test_per_edge_marker_round_trip(tmp_path, sga):
     sga.autosage_cache_clear()
 
 
+def test_hybrid_schedule_round_trip(tmp_path, sga):
+    # the ELL + CSR schedule family is stored by name like the others
+    sga.autosage_cache_clear()
+    line = "NVIDIA_GB300|sm152|op0|dt0|F4|H1|n10|m10|nnz20|fp00000000000000ab\thybrid 1 4 512 0.050000\n"
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + line)
+    sga.autosage_cache_load(str(p))
+    assert sga.autosage_cache_size() == 1
+    q = tmp_path / "d.txt"
+    sga.autosage_cache_save(str(q))
+    assert q.read_text() == HEADER + line
+    sga.autosage_cache_clear()
+
+
 def test_wrong_header_rejected(tmp_path, sga):
     sga.autosage_cache_clear()
     p = tmp_path / "c.txt"

@@ -43,6 +43,8 @@ SCHEDULES = [
 SPMM_SCHEDULES = SCHEDULES + [
     ("mergepath-32", dict(kind=sga.SCHED_MERGEPATH, split=32)),
     ("mergepath-300", dict(kind=sga.SCHED_MERGEPATH, split=300)),
+    ("hybrid-32", dict(kind=sga.SCHED_HYBRID, split=32)),
+    ("hybrid-512-e4", dict(kind=sga.SCHED_HYBRID, split=512, lanes_e=4)),
 ]
 
 
@@ -307,7 +309,7 @@ def edge_case_graphs():
 
 
 @pytest.mark.parametrize("name,g", edge_case_graphs(), ids=[e[0] for e in edge_case_graphs()])
-@pytest.mark.parametrize("sched", ["default", "split", "mergepath", "binned"])
+@pytest.mark.parametrize("sched", ["default", "split", "mergepath", "binned", "hybrid"])
 def test_edge_cases(name, g, sched):
     A = mat(g)
     F = 6
@@ -315,11 +317,12 @@ def test_edge_cases(name, g, sched):
     Q = synth.normal(g.n_rows, F, 11, synth.STREAM_Q)
     K = synth.normal(g.n_cols, F, 11, synth.STREAM_K)
     spec = {"default": None, "split": dict(kind=sga.SCHED_SPLIT, split=2),
-            "mergepath": dict(kind=sga.SCHED_MERGEPATH, split=3), "binned": dict(kind=sga.SCHED_BINNED, split=2)}[sched]
+            "mergepath": dict(kind=sga.SCHED_MERGEPATH, split=3), "binned": dict(kind=sga.SCHED_BINNED, split=2),
+            "hybrid": dict(kind=sga.SCHED_HYBRID, split=8)}[sched]
     plan = make_plan(A, sga.OP_SPMM, F, spec)
     Y = sga.autosage_spmm(A, dev(X), plan=plan)
     assert_close(to_np(Y), oracle.spmm(g.row_ptr, g.col_idx, g.vals, X), TOL_F32, f"{name} spmm")
-    if sched == "mergepath":
+    if sched in ("mergepath", "hybrid"):  # SpMM-only schedule families
         return
     plan = make_plan(A, sga.OP_SDDMM, F, spec)
     S = sga.autosage_sddmm(A, dev(Q), dev(K), plan=plan)
@@ -370,7 +373,7 @@ def test_repeat_runs_are_bitwise_identical(skew, name, spec):
     first = sga.autosage_spmm(A, X, plan=plan).clone()
     for _ in range(3):
         assert torch.equal(sga.autosage_spmm(A, X, plan=plan), first)
-    if spec["kind"] != sga.SCHED_MERGEPATH:
+    if spec["kind"] not in (sga.SCHED_MERGEPATH, sga.SCHED_HYBRID):  # SpMM-only families
         aplan = make_plan(A, sga.OP_ATTN, 16, spec, heads=4)
         Q = dev(synth.normal(g.n_rows, 64, 12, synth.STREAM_Q))
         o1 = sga.autosage_csr_attention(A, Q, Q, X, 4, 0.25, plan=aplan).clone()
