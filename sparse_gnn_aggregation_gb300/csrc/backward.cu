@@ -34,17 +34,21 @@ namespace {
 constexpr float kRescaleB = 8.f;
 
 // Edges in flight per edge lane: two while a lane's Q and dO fragments take
-// at most 32 bytes each (bf16 up to 16 values, fp32 up to 8), else one.
+// less than 32 bytes each, else one.
 template <typename T, int VW, int NV>
 __host__ __device__ constexpr int bwd_unroll() {
-  return NV * VW * (int)sizeof(T) <= 32 ? 2 : 1;
+  return NV * VW * (int)sizeof(T) < 32 ? 2 : 1;
 }
 
-// Blocks per SM the register budget is sized for: lanes holding at most 16
+// Blocks per SM the register budget is sized for: lanes holding at most 32
 // bytes of a row fit three 256-thread blocks (85 registers), wider ones two.
+// The pass is bound by memory latency, so occupancy wins over edges in
+// flight per lane (measured on R-MAT scale 20, bf16, H = 8, D = 64: three
+// blocks with one edge in flight 12.0 ms against two blocks with two edges
+// 12.5 ms).
 template <typename T, int VW, int NV>
 constexpr int bwd_min_blocks() {
-  return NV * VW * (int)sizeof(T) <= 16 ? 3 : 2;
+  return NV * VW * (int)sizeof(T) <= 32 ? 3 : 2;
 }
 
 // Per-chunk state layout in `part`: [n_chunks][2][width] for (A, B), then
