@@ -41,10 +41,14 @@ cudaError_t launch_spmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                         void *Y, int64_t ldy, const ChunkList &cl, float *partial,
                         cudaStream_t s);
 
-// SDDMM: S[p*H + h] = alpha * <Q[row, h], K[col, h]>.
+// SDDMM: S[p*H + h] = alpha * <Q[row, h], K[col, h]>. Items come from the
+// chunk list's deal, or (mp_part != null) from a merge path: lane group w
+// takes diagonals [mp_part[w], mp_part[w + 1]) of the (rows + edges) path,
+// n_groups groups.
 cudaError_t launch_sddmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const void *Q, int64_t ldq, const void *K,
-                         int64_t ldk, float alpha, float *S, const ChunkList &cl, cudaStream_t s);
+                         int64_t ldk, float alpha, float *S, const ChunkList &cl, const int2 *mp_part,
+                         int64_t n_groups, cudaStream_t s);
 
 // Row softmax in place on S [nnz, H]. ml: [n_chunks * H * 2] fp32 workspace,
 // row_ml: [n_long * H * 2] fp32 workspace (only with cut rows).

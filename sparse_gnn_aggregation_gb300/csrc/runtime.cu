@@ -488,9 +488,10 @@ autosage_status build_workspace(autosage_plan_s *P, cudaStream_t s) {
                          P->ell_col.as<int32_t>(), P->ell_start.as<int32_t>(), s));
     }
   } else if (P->sched.kind == AUTOSAGE_SCHED_MERGEPATH) {
-    if (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)
-      return fail(AUTOSAGE_ERR_UNSUPPORTED, "merge-path schedule is SpMM only");
-    st = build_mergepath(P, P->sched.split, P->F, s);
+    if (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T && P->op != AUTOSAGE_OP_SDDMM)
+      return fail(AUTOSAGE_ERR_UNSUPPORTED, "merge-path schedule is SpMM and SDDMM only");
+    // SDDMM writes one value per edge: its merge path needs partitions but no carries
+    st = build_mergepath(P, P->sched.split, P->op == AUTOSAGE_OP_SDDMM ? 0 : P->F, s);
   }
   if (st != AUTOSAGE_OK) return st;
   if ((P->op == AUTOSAGE_OP_ATTN_UNFUSED || P->op == AUTOSAGE_OP_ATTN_BACKWARD) && !P->scores.p)
@@ -604,7 +605,9 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
       st = choose_geom(P->dt, 1, P->F, {{a.Q, a.ldq}, {a.K, a.ldk}}, P->sched.G, P->sched.E, true, 16, g);
       if (st != AUTOSAGE_OK) return st;
       if (P->sched.pe) g.batched = false;
-      e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, a.ldq, a.K, a.ldk, a.alpha, a.S, cl, s);
+      const bool mp = P->sched.kind == AUTOSAGE_SCHED_MERGEPATH;
+      e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, a.ldq, a.K, a.ldk, a.alpha, a.S, cl,
+                       mp ? P->mp_part.as<int2>() : nullptr, mp ? P->mp_warps : 0, s);
       break;
     }
     case AUTOSAGE_OP_SOFTMAX: {
@@ -646,7 +649,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
       float *S = a.S;
       st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.K, ld}}, P->sched.G, P->sched.E, true, 16, g);
       if (st == AUTOSAGE_OK) {
-        e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, ld, a.K, ld, a.alpha, S, cl, s);
+        e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, a.Q, ld, a.K, ld, a.alpha, S, cl, nullptr, 0, s);
       } else if (st == AUTOSAGE_ERR_UNSUPPORTED && P->H > 1) {
         const size_t es = dtype_size(P->dt);
         for (int h = 0; h < P->H && e == cudaSuccess; ++h) {
@@ -655,7 +658,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
           st = choose_geom(P->dt, 1, P->F, {{q, ld}, {k, ld}}, P->sched.G, P->sched.E, true, 16, g);
           if (st != AUTOSAGE_OK) return st;
           g.es = P->H;
-          e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, q, ld, k, ld, a.alpha, S + h, cl, s);
+          e = launch_sddmm(g, wk.rows, wk.row_ptr, wk.col_idx, q, ld, k, ld, a.alpha, S + h, cl, nullptr, 0, s);
         }
       } else {
         return st;
@@ -1002,7 +1005,7 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
           out.push_back({hy, estimate(dev, st, P->op, P->dt, P->F, sh.H, hy, g) * 0.97});
         }
       }
-      if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && G * E == 32) {
+      if (((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && G * E == 32) || P->op == AUTOSAGE_OP_SDDMM) {
         for (int items : {256, 1024}) {
           Sched mp{AUTOSAGE_SCHED_MERGEPATH, G, E, items};
           out.push_back({mp, estimate(dev, st, P->op, P->dt, P->F, sh.H, mp, g)});
@@ -1053,7 +1056,8 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
     if (P->op != AUTOSAGE_OP_SDDMM || x.G < 4) x.pe = 0;
     if (softmax && x.E != 1) return;
     if (x.kind == AUTOSAGE_SCHED_MERGEPATH) {
-      if (x.G * x.E != 32 || (P->op != AUTOSAGE_OP_SPMM && P->op != AUTOSAGE_OP_SPMM_T)) return;
+      const bool spmm = P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T;
+      if ((spmm && x.G * x.E != 32) || (!spmm && P->op != AUTOSAGE_OP_SDDMM)) return;
       if (x.split < 64 || x.split > 16384) return;
     } else if (x.kind == AUTOSAGE_SCHED_SPLIT) {
       if (x.split < 16 || x.split >= maxd) return;
@@ -1070,10 +1074,11 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
   };
   for (int e2 : {E / 2, E * 2}) {
     if (e2 < 1 || e2 > 32) continue;
-    // merge path keeps whole warps: the feature lanes follow the edge lanes
-    add(Sched{b.kind, b.kind == AUTOSAGE_SCHED_MERGEPATH ? 32 / e2 : G, e2, b.split, b.pe});
+    // SpMM's merge path keeps whole warps: the feature lanes follow the edge lanes
+    const bool whole = b.kind == AUTOSAGE_SCHED_MERGEPATH && P->op != AUTOSAGE_OP_SDDMM;
+    add(Sched{b.kind, whole ? 32 / e2 : G, e2, b.split, b.pe});
   }
-  if (b.kind != AUTOSAGE_SCHED_MERGEPATH && !softmax)
+  if ((b.kind != AUTOSAGE_SCHED_MERGEPATH || P->op == AUTOSAGE_OP_SDDMM) && !softmax)
     for (int g2 : {G / 2, G * 2})
       if (g2 >= 1) add(Sched{b.kind, g2, E, b.split, b.pe});
   if (b.kind != AUTOSAGE_SCHED_ROWGROUP)

@@ -21,19 +21,39 @@ namespace {
 
 // Per-edge reduction. Fragment slot k of lane g is fragment g * fs + k * ks.
 // ONE: all slots of a lane belong to one head; otherwise slot k is its own head.
-template <typename T, int VW, int NV, bool ONE>
+// Items of an SDDMM launch: dealt from the run table (MP = false), or (MP =
+// true) a merge path: lane group w walks its equal share of (rows + edges),
+// diagonals [part[w], part[w + 1]), one item per row it touches. SDDMM writes
+// one value per edge, so a row cut between groups needs no carry.
+template <bool MP, typename Body>
+__device__ __forceinline__ void for_items(const Lanes &L, int64_t n_rows, const int32_t *__restrict__ row_ptr,
+                                          const ChunkList &cl, int ipb, const int2 *__restrict__ part,
+                                          int64_t n_groups, Body body) {
+  if constexpr (MP) {
+    const int64_t w = ((int64_t)blockIdx.x * (kBlock / 32) + (threadIdx.x >> 5)) * (32 / L.GE) + L.slot;
+    if (w >= n_groups) return;  // the whole group leaves together
+    const int2 s0 = part[w], s1 = part[w + 1];
+    for (int64_t i = s0.x; i <= s1.x && i < n_rows; ++i) {
+      const int b = max(row_ptr[i], s0.y), e = min(row_ptr[i + 1], s1.y);
+      if (e > b) body(Item{i, b, e, -1, true});
+    }
+  } else {
+    __shared__ int s_items;
+    const ItemQueue queue(n_rows, cl, ipb, &s_items);
+    int64_t idx;
+    while (queue.next(L, idx)) body(item_at(idx, n_rows, row_ptr, cl));
+  }
+}
+
+template <typename T, int VW, int NV, bool ONE, bool MP>
 __global__ void __launch_bounds__(kBlock) sddmm_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha,
     int H, int es, int cph, int R, int nfrag, int G, int E, int fs, int ks, float *__restrict__ S,
-    ChunkList cl, int ipb) {
+    ChunkList cl, int ipb, const int2 *__restrict__ mp_part, int64_t n_groups) {
   constexpr int NG = ONE ? 1 : NV;
   const Lanes L(G, E);
-  __shared__ int s_items;
-  const ItemQueue queue(n_rows, cl, ipb, &s_items);
-  int64_t idx;
-  while (queue.next(L, idx)) {
-  const Item it = item_at(idx, n_rows, row_ptr, cl);
+  for_items<MP>(L, n_rows, row_ptr, cl, ipb, mp_part, n_groups, [&](const Item &it) {
   const int g = L.g;
   int frag[NV];
 #pragma unroll
@@ -98,7 +118,7 @@ __global__ void __launch_bounds__(kBlock) sddmm_kernel(
       }
     }
   }
-  }
+  });
 }
 
 // Batched single-head SDDMM: each edge lane's G feature lanes take B edges
@@ -106,21 +126,18 @@ __global__ void __launch_bounds__(kBlock) sddmm_kernel(
 // edges; a transpose-reduction inside each aligned B-lane segment (B - 1
 // shuffles) leaves edge j's segment sum on lane j of the segment, and log2(G/B)
 // plain xor rounds add the segments. Lanes 0..B-1 then hold the B scores.
-template <typename T, int VW, int NV, int B>
+template <typename T, int VW, int NV, int B, bool MP>
 __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const T *__restrict__ Q, int64_t ldq, const T *__restrict__ K, int64_t ldk, float alpha, int es,
-    int nfrag, int G, int E, float *__restrict__ S, ChunkList cl, int ipb) {
+    int nfrag, int G, int E, float *__restrict__ S, ChunkList cl, int ipb, const int2 *__restrict__ mp_part,
+    int64_t n_groups) {
   const Lanes L(G, E);
   const int g = L.g;
   const int base_lane = L.slot * L.GE + L.e * G;  // lane 0 of this edge lane's segment
   // loads of the whole batch in flight when a lane holds at most two fragments
   constexpr int U = NV <= 2 ? B : (B < 4 ? B : 4);
-  __shared__ int s_items;
-  const ItemQueue queue(n_rows, cl, ipb, &s_items);
-  int64_t idx;
-  while (queue.next(L, idx)) {
-    const Item it = item_at(idx, n_rows, row_ptr, cl);
+  for_items<MP>(L, n_rows, row_ptr, cl, ipb, mp_part, n_groups, [&](const Item &it) {
     Frag<T, VW> q[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
@@ -179,22 +196,26 @@ __global__ void __launch_bounds__(kBlock) sddmm_batched_kernel(
       for (int off = B; off < G; off <<= 1) part[0] += __shfl_xor_sync(L.sub_mask, part[0], off);
       if (g < nb) S[(int64_t)pj * es] = alpha * part[0];
     }
-  }
+  });
 }
 
 template <typename T, int VW, int NV>
 cudaError_t launch_batched(const Geom &g, int64_t grid, int ipb, int64_t n_rows, const int32_t *row_ptr,
                            const int32_t *col_idx, const T *Q, int64_t ldq, const T *K, int64_t ldk,
-                           float alpha, float *S, const ChunkList &cl, cudaStream_t s) {
-#define AUTOSAGE_SDDMM_B(BB)                                                                              \
-  sddmm_batched_kernel<T, VW, NV, BB><<<(unsigned)grid, kBlock, 0, s>>>(                                \
-      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.G, g.E, S, cl, ipb)
-  if (g.G >= 8)
-    AUTOSAGE_SDDMM_B(8);
-  else if (g.G == 4)
-    AUTOSAGE_SDDMM_B(4);
-  else
+                           float alpha, float *S, const ChunkList &cl, const int2 *mp_part, int64_t n_groups,
+                           cudaStream_t s) {
+#define AUTOSAGE_SDDMM_B(BB, MPP)                                                                         \
+  sddmm_batched_kernel<T, VW, NV, BB, MPP><<<(unsigned)grid, kBlock, 0, s>>>(                           \
+      n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.es, g.nfrag, g.G, g.E, S, cl, ipb, mp_part, n_groups)
+  if (g.G >= 8) {
+    if (mp_part) AUTOSAGE_SDDMM_B(8, true);
+    else AUTOSAGE_SDDMM_B(8, false);
+  } else if (g.G == 4) {
+    if (mp_part) AUTOSAGE_SDDMM_B(4, true);
+    else AUTOSAGE_SDDMM_B(4, false);
+  } else {
     return cudaErrorInvalidValue;
+  }
 #undef AUTOSAGE_SDDMM_B
   return cudaGetLastError();
 }
@@ -202,29 +223,34 @@ cudaError_t launch_batched(const Geom &g, int64_t grid, int ipb, int64_t n_rows,
 template <typename T, int VW>
 cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
                      const T *Q, int64_t ldq, const T *K, int64_t ldk, float alpha, float *S,
-                     const ChunkList &cl_in, cudaStream_t s) {
+                     const ChunkList &cl_in, const int2 *mp_part, int64_t n_groups, cudaStream_t s) {
   const Deal dl = deal_items(cl_in, n_rows, g.G * g.E, g.G);
   const ChunkList &cl = dl.cl;
   const int ipb = dl.ipb;
-  const int64_t grid = dl.grid;
+  // merge path: one lane group per partition, 256 / (G * E) groups per block
+  const int64_t gpb = (int64_t)(kBlock / 32) * (32 / (g.G * g.E));
+  const int64_t grid = mp_part ? (n_groups + gpb - 1) / gpb : dl.grid;
   if (grid <= 0) return cudaSuccess;
   // batched transpose-reduction: single head, 16-byte fragments, 2..32 lanes
   if constexpr (sizeof(T) * VW == 16) {
     if (g.H == 1 && g.batched && g.G >= 2 && g.fs == 1 && g.NV <= 4) {
       switch (g.NV) {
-        case 1: return launch_batched<T, VW, 1>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, s);
-        case 2: return launch_batched<T, VW, 2>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, s);
-        case 4: return launch_batched<T, VW, 4>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, s);
+        case 1: return launch_batched<T, VW, 1>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, mp_part, n_groups, s);
+        case 2: return launch_batched<T, VW, 2>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, mp_part, n_groups, s);
+        case 4: return launch_batched<T, VW, 4>(g, grid, ipb, n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, S, cl, mp_part, n_groups, s);
       }
     }
   }
-#define AUTOSAGE_SDDMM(NVV, ONEG)                                                                     \
-  sddmm_kernel<T, VW, NVV, ONEG><<<(unsigned)grid, kBlock, 0, s>>>(                                 \
+#define AUTOSAGE_SDDMM2(NVV, ONEG, MPP)                                                              \
+  sddmm_kernel<T, VW, NVV, ONEG, MPP><<<(unsigned)grid, kBlock, 0, s>>>(                            \
       n_rows, row_ptr, col_idx, Q, ldq, K, ldk, alpha, g.H, g.es, g.cph, g.R, g.nfrag, g.G, g.E,     \
-      g.fs, g.ks, S, cl, ipb)
-#define AUTOSAGE_SDDMM_NV(NVV)              \
-  if (g.one) AUTOSAGE_SDDMM(NVV, true);     \
-  else AUTOSAGE_SDDMM(NVV, false);
+      g.fs, g.ks, S, cl, ipb, mp_part, n_groups)
+#define AUTOSAGE_SDDMM(NVV, ONEG)                      \
+  if (mp_part) AUTOSAGE_SDDMM2(NVV, ONEG, true);       \
+  else AUTOSAGE_SDDMM2(NVV, ONEG, false);
+#define AUTOSAGE_SDDMM_NV(NVV)                \
+  if (g.one) { AUTOSAGE_SDDMM(NVV, true) }    \
+  else { AUTOSAGE_SDDMM(NVV, false) }
   switch (g.NV) {
     case 1: AUTOSAGE_SDDMM_NV(1); break;
     case 2: AUTOSAGE_SDDMM_NV(2); break;
@@ -235,6 +261,7 @@ cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, cons
   }
 #undef AUTOSAGE_SDDMM_NV
 #undef AUTOSAGE_SDDMM
+#undef AUTOSAGE_SDDMM2
   return cudaGetLastError();
 }
 
@@ -242,23 +269,24 @@ cudaError_t sddmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, cons
 
 cudaError_t launch_sddmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const void *Q, int64_t ldq, const void *K,
-                         int64_t ldk, float alpha, float *S, const ChunkList &cl, cudaStream_t s) {
+                         int64_t ldk, float alpha, float *S, const ChunkList &cl, const int2 *mp_part,
+                         int64_t n_groups, cudaStream_t s) {
   if (g.dt == DType::F32) {
     auto q = static_cast<const float *>(Q);
     auto k = static_cast<const float *>(K);
     switch (g.VW) {
-      case 4: return sddmm_vw<float, 4>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
-      case 2: return sddmm_vw<float, 2>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
-      case 1: return sddmm_vw<float, 1>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
+      case 4: return sddmm_vw<float, 4>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
+      case 2: return sddmm_vw<float, 2>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
+      case 1: return sddmm_vw<float, 1>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
     }
   } else {
     auto q = static_cast<const __nv_bfloat16 *>(Q);
     auto k = static_cast<const __nv_bfloat16 *>(K);
     switch (g.VW) {
-      case 8: return sddmm_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
-      case 4: return sddmm_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
-      case 2: return sddmm_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
-      case 1: return sddmm_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, s);
+      case 8: return sddmm_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
+      case 4: return sddmm_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
+      case 2: return sddmm_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
+      case 1: return sddmm_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, q, ldq, k, ldk, alpha, S, cl, mp_part, n_groups, s);
     }
   }
   return cudaErrorInvalidValue;

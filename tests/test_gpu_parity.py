@@ -165,7 +165,8 @@ def test_spmm_transpose(skew, name, spec):
 
 # ---------------------------------------------------------------- SDDMM
 
-@pytest.mark.parametrize("name,spec", SCHEDULES, ids=[s[0] for s in SCHEDULES])
+@pytest.mark.parametrize("name,spec", SCHEDULES + [("mergepath-64", dict(kind=sga.SCHED_MERGEPATH, split=64))],
+                         ids=[s[0] for s in SCHEDULES] + ["mergepath-64"])
 def test_sddmm_tiny_er(tiny, name, spec):
     g, _, Q, K, _ = tiny
     A = mat(g)
@@ -174,8 +175,16 @@ def test_sddmm_tiny_er(tiny, name, spec):
     assert_close(to_np(S), oracle.sddmm(g.row_ptr, g.col_idx, Q, K, 1.0)[:, 0], TOL_F32, f"sddmm {name}")
 
 
+# merge path for SDDMM: lane groups of any shape walk equal shares of (rows + edges)
+SDDMM_SCHEDULES = SCHEDULES + [
+    ("mergepath-32", dict(kind=sga.SCHED_MERGEPATH, split=32)),
+    ("mergepath-300-e2", dict(kind=sga.SCHED_MERGEPATH, split=300, lanes_e=2)),
+    ("mergepath-1024-pe", dict(kind=sga.SCHED_MERGEPATH, split=1024, per_edge=1)),
+]
+
+
 @pytest.mark.parametrize("F", [1, 3, 4, 8, 16, 32, 64, 100, 128, 256])
-@pytest.mark.parametrize("name,spec", SCHEDULES, ids=[s[0] for s in SCHEDULES])
+@pytest.mark.parametrize("name,spec", SDDMM_SCHEDULES, ids=[s[0] for s in SDDMM_SCHEDULES])
 def test_sddmm_width_sweep_skewed(skew, F, name, spec):
     g = skew
     A = mat(g)
@@ -322,11 +331,12 @@ def test_edge_cases(name, g, sched):
     plan = make_plan(A, sga.OP_SPMM, F, spec)
     Y = sga.autosage_spmm(A, dev(X), plan=plan)
     assert_close(to_np(Y), oracle.spmm(g.row_ptr, g.col_idx, g.vals, X), TOL_F32, f"{name} spmm")
-    if sched in ("mergepath", "hybrid"):  # SpMM-only schedule families
+    if sched != "hybrid":  # SpMM only
+        plan = make_plan(A, sga.OP_SDDMM, F, spec)
+        S = sga.autosage_sddmm(A, dev(Q), dev(K), plan=plan)
+        assert_close(to_np(S), oracle.sddmm(g.row_ptr, g.col_idx, Q, K)[:, 0], TOL_F32, f"{name} sddmm")
+    if sched in ("mergepath", "hybrid"):  # the attention ops take neither family
         return
-    plan = make_plan(A, sga.OP_SDDMM, F, spec)
-    S = sga.autosage_sddmm(A, dev(Q), dev(K), plan=plan)
-    assert_close(to_np(S), oracle.sddmm(g.row_ptr, g.col_idx, Q, K)[:, 0], TOL_F32, f"{name} sddmm")
     for fused in (True, False):
         plan = make_plan(A, sga.OP_ATTN if fused else sga.OP_ATTN_UNFUSED, F, spec)
         O = sga.autosage_csr_attention(A, dev(Q), dev(K), dev(X), 1, 0.7, fused=fused, plan=plan)
