@@ -69,7 +69,8 @@ typedef enum {
   AUTOSAGE_SCHED_SPLIT = 1,      /* rows longer than `split` edges are cut into chunks whose
                                     partial results are combined in a fixed order */
   AUTOSAGE_SCHED_MERGEPATH = 2,  /* equal (rows + edges) share per warp along the merge path,
-                                    carry-out of rows cut at warp boundaries, fixed-order fix-up */
+                                    carry-out of rows cut at warp boundaries, fixed-order fix-up
+                                    (SpMM); SDDMM: an equal share per lane group, no carries */
   AUTOSAGE_SCHED_BINNED = 3,     /* SPLIT, with rows taken in order of degree bucket (longest
                                     first) so the lane groups of a warp get rows of similar length */
   AUTOSAGE_SCHED_HYBRID = 4      /* SpMM only: BINNED for rows of 8 or more edges, and the rows of

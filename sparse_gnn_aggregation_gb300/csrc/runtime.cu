@@ -573,10 +573,14 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
       const bool mp = P->sched.kind == AUTOSAGE_SCHED_MERGEPATH;
       const int E_req = mp ? 0 : P->sched.E;
       // lanes and fragment width for the full row; rows wider than one pass
-      // (NV > 16 fragments per lane) are cut into column tiles of 16 * G * VW
+      // (NV > 16 fragments per lane) are cut into column tiles of 8 * G * VW,
+      // run one after another: eight fragments a lane keep two edges in
+      // flight (measured on the Reddit-like graph at F = 602: the probes then
+      // choose merge path G = 16, E = 2 at 48.7 ms, against 62.6 ms with
+      // tiles of 16 fragments)
       st = choose_geom(P->dt, 1, P->F, {{a.X, a.ldx}, {a.Y, a.ldy}}, P->sched.G, E_req, false, 1 << 20, g);
       if (st != AUTOSAGE_OK) return st;
-      const int64_t tile = (int64_t)16 * g.G * g.VW;
+      const int64_t tile = (int64_t)(g.NV > 16 ? 8 : 16) * g.G * g.VW;
       const size_t es = dtype_size(P->dt);
       for (int64_t off = 0; off < P->F && e == cudaSuccess; off += tile) {
         const int64_t w = std::min<int64_t>(tile, P->F - off);
@@ -903,31 +907,39 @@ bool fault(const char *name) {
   return f && strcmp(f, name) == 0;
 }
 
-// Time one schedule: 1 warm-up, then `reps` timed runs; median in ms.
+// Time one schedule: 1 warm-up, then `reps` timed runs, each after an
+// overwrite of the L2-sized flush buffer, issued back to back (one host
+// synchronisation at the end, as the operations of a step run); median in ms.
 autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &ms, cudaStream_t s) {
   if (fault("probe_fail")) return fail(AUTOSAGE_ERR_PROBE, "probe failure injected (AUTOSAGE_FAULT=probe_fail)");
-  std::vector<float> t;
-  cudaEvent_t e0, e1;
-  CUDA_TRY(cudaEventCreate(&e0));
-  CUDA_TRY(cudaEventCreate(&e1));
+  std::vector<cudaEvent_t> ev(2 * (size_t)(reps + 1), nullptr);
+  autosage_status st = AUTOSAGE_OK;
+  for (cudaEvent_t &e : ev)
+    if (st == AUTOSAGE_OK && cudaEventCreate(&e) != cudaSuccess) st = fail(AUTOSAGE_ERR_CUDA, "probe events");
   OpArgs a = pb.a;
   if (P->op == AUTOSAGE_OP_ATTN_UNFUSED) a.S = P->scores.as<float>();
-  autosage_status st = AUTOSAGE_OK;
   for (int r = 0; r <= reps && st == AUTOSAGE_OK; ++r) {
     if (P->op == AUTOSAGE_OP_SOFTMAX)
       cudaMemcpyAsync(pb.Y.p, pb.S.p, (size_t)pb.out_elems * 4, cudaMemcpyDeviceToDevice, s);
     if (pb.flush.p) cudaMemsetAsync(pb.flush.p, r & 0xff, pb.flush.bytes, s);
-    cudaEventRecord(e0, s);
+    cudaEventRecord(ev[2 * r], s);
     st = run_op(P, P->op, &P->a0, a, s);
-    cudaEventRecord(e1, s);
-    cudaError_t e = cudaEventSynchronize(e1);
-    if (e != cudaSuccess) st = cuda_fail(e, "probe");
-    float x = 0;
-    cudaEventElapsedTime(&x, e0, e1);
-    if (r > 0) t.push_back(x);
+    cudaEventRecord(ev[2 * r + 1], s);
   }
-  cudaEventDestroy(e0);
-  cudaEventDestroy(e1);
+  std::vector<float> t;
+  if (st == AUTOSAGE_OK) {
+    const cudaError_t e = cudaEventSynchronize(ev.back());
+    if (e != cudaSuccess) st = cuda_fail(e, "probe");
+    for (int r = 1; r <= reps && st == AUTOSAGE_OK; ++r) {
+      float x = 0;
+      cudaEventElapsedTime(&x, ev[2 * r], ev[2 * r + 1]);
+      t.push_back(x);
+    }
+  } else {
+    cudaStreamSynchronize(s);
+  }
+  for (cudaEvent_t e : ev)
+    if (e) cudaEventDestroy(e);
   if (st != AUTOSAGE_OK) return st;
   std::sort(t.begin(), t.end());
   ms = t[t.size() / 2];
@@ -956,10 +968,10 @@ bool cand_geom(const autosage_plan_s *P, int G, int E, Geom &g) {
   g = Geom{};
   g.dt = P->dt; g.H = sh.H; g.D = sh.D; g.VW = vb / s; g.nfrag = (int)nfrag; g.G = G; g.E = E;
   g.NV = pow2ceil((nfrag + G - 1) / G);
-  // SpMM runs rows wider than 16 fragments per lane as column tiles of 16
+  // SpMM runs rows wider than 16 fragments per lane as column tiles of 8
   // fragments per lane, one launch after another: each launch is a candidate
   // of that geometry
-  if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && g.NV > 16) g.NV = 16;
+  if ((P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T) && g.NV > 16) g.NV = 8;
   return g.NV <= sh.nv_max;
 }
 
@@ -1376,21 +1388,36 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
     };
     for (const Candidate &c : top) probe_one(c);
     // local refinement: the estimate ranks edge lanes and chunk lengths
-    // poorly, so the neighbours of the fastest schedule are probed too, and
-    // again around each new fastest one (at most four rounds)
-    // (separately for each reduction form: their best lane counts differ)
-    std::vector<Sched> tried;
+    // poorly, so the neighbours of the fastest schedules are probed too: each
+    // round expands the three fastest schedules of a reduction form that were
+    // not expanded yet (a beam, since the best schedule can be two steps away
+    // through a slightly slower one), at most four rounds, stopping when a
+    // round finds nothing faster (separately for each reduction form: their
+    // best lane counts differ)
+    std::vector<Sched> tried, expanded;
+    auto seen = [](const std::vector<Sched> &v, const Sched &x) {
+      return std::any_of(v.begin(), v.end(), [&](const Sched &t) { return same_sched(t, x); });
+    };
     for (const Candidate &c : top) tried.push_back(c.sc);
     for (int f = 0; f < 2; ++f) {
       for (int round = 0; round < 4 && form_ms[f] >= 0; ++round) {
-        const Sched centre = form_best[f];
-        for (const Candidate &c : neighbours(dev, P, rs, centre)) {
-          if ((c.sc.pe ? 1 : 0) != f) continue;
-          if (std::any_of(tried.begin(), tried.end(), [&](const Sched &t) { return same_sched(t, c.sc); })) continue;
-          tried.push_back(c.sc);
-          probe_one(c);
+        const double before = form_ms[f];
+        std::vector<std::pair<double, Sched>> beam;
+        for (const auto &pc : passed)
+          if ((pc.second.sc.pe ? 1 : 0) == f && !seen(expanded, pc.second.sc)) beam.push_back({pc.first, pc.second.sc});
+        std::stable_sort(beam.begin(), beam.end(), [](const std::pair<double, Sched> &x,
+                                                      const std::pair<double, Sched> &y) { return x.first < y.first; });
+        if (beam.size() > 3) beam.resize(3);
+        if (beam.empty()) break;
+        for (const auto &centre : beam) {
+          expanded.push_back(centre.second);
+          for (const Candidate &c : neighbours(dev, P, rs, centre.second)) {
+            if ((c.sc.pe ? 1 : 0) != f || seen(tried, c.sc)) continue;
+            tried.push_back(c.sc);
+            probe_one(c);
+          }
         }
-        if (same_sched(form_best[f], centre)) break;
+        if (!(form_ms[f] < before)) break;
       }
     }
     // final round: the three fastest schedules timed again with more runs, so
