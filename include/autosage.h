@@ -87,6 +87,9 @@ typedef struct {
   int per_edge;    /* SDDMM with one head: 1 = finish each edge's dot product with its own
                       shuffle reduction; 0 = lane groups of 4 or more lanes reduce batches of
                       4 or 8 edges with one transpose-reduction. Other ops ignore it. */
+  int lanes_f_agg; /* unfused attention: feature lanes of the aggregation stage (the SpMM
+                      with the softmax weights; power of two, lanes_f_agg * lanes_e <= 32);
+                      0 = lanes_f. The score stage uses lanes_f. Must be 0 for other ops. */
 } autosage_schedule;
 
 /* A CSR matrix in device memory. Rows are destinations, col_idx are sources.

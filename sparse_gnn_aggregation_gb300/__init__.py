@@ -57,7 +57,7 @@ class _Csr(ctypes.Structure):
 
 class _Schedule(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("lanes_f", ctypes.c_int), ("lanes_e", ctypes.c_int),
-                ("split", ctypes.c_int), ("per_edge", ctypes.c_int)]
+                ("split", ctypes.c_int), ("per_edge", ctypes.c_int), ("lanes_f_agg", ctypes.c_int)]
 
 
 def _load():
@@ -240,7 +240,7 @@ class Plan:
         ms = ctypes.c_double()
         _check(_lib.autosage_plan_schedule(self.handle, ctypes.byref(s), ctypes.byref(ms)))
         return {"kind": s.kind, "lanes_f": s.lanes_f, "lanes_e": s.lanes_e, "split": s.split,
-                "per_edge": s.per_edge, "probe_ms": ms.value}
+                "per_edge": s.per_edge, "lanes_f_agg": s.lanes_f_agg, "probe_ms": ms.value}
 
     def rebind(self, A: "CsrMatrix", stream=None):
         """Bind the plan to a copy of its graph's structure in other device memory
@@ -277,10 +277,11 @@ def autosage_plan(A: CsrMatrix, op: int, F: int, heads: int = 1, dtype=None, fla
 
 
 def autosage_plan_with_schedule(A: CsrMatrix, op: int, F: int, kind: int, lanes_f: int = 0, lanes_e: int = 0,
-                                split: int = 0, heads: int = 1, dtype=None, stream=None, per_edge: int = 0) -> Plan:
+                                split: int = 0, heads: int = 1, dtype=None, stream=None, per_edge: int = 0,
+                                lanes_f_agg: int = 0) -> Plan:
     torch = _torch()
     dt = BF16 if dtype == torch.bfloat16 else F32
-    s = _Schedule(kind, lanes_f, lanes_e, split, int(bool(per_edge)))
+    s = _Schedule(kind, lanes_f, lanes_e, split, int(bool(per_edge)), int(lanes_f_agg))
     h = ctypes.c_void_p()
     _check(_lib.autosage_plan_with_schedule(A.c, op, int(F), int(heads), dt, ctypes.byref(s), ctypes.byref(h),
                                             _stream(stream)))

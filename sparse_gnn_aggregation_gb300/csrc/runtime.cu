@@ -246,6 +246,7 @@ struct Sched {
   int kind = AUTOSAGE_SCHED_ROWGROUP;
   int G = 0, E = 0, split = 0;
   int pe = 0;  // SDDMM, one head: per-edge shuffle reductions instead of batched ones
+  int G2 = 0;  // unfused attention: feature lanes of the aggregation stage (0: G)
 };
 
 }  // namespace
@@ -671,7 +672,11 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
       e = launch_row_softmax(wk.rows, wk.row_ptr, P->H, S, cl, P->ml.as<float>(), P->row_ml.as<float>(), s);
       if (e != cudaSuccess) break;
       Geom g2;
-      st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, P->sched.G, P->sched.E, false, 16, g2);
+      // the aggregation stage has its own feature lanes (measured on R-MAT scale 20,
+      // bf16, H = 8, D = 64: scores at 16 lanes and aggregation at 32 ran 5.74 ms,
+      // both at 16 6.37 ms)
+      const int G_agg = P->sched.G2 > 0 ? P->sched.G2 : P->sched.G;
+      st = choose_geom(P->dt, P->H, P->F, {{a.X, ld}, {a.Y, ld}}, G_agg, P->sched.E, false, 16, g2);
       if (st != AUTOSAGE_OK) return st;
       e = launch_spmm(g2, wk.rows, wk.row_ptr, wk.col_idx, S, a.X, ld, a.Y, ld, cl,
                       P->partial.as<float>(), s);
@@ -947,7 +952,7 @@ autosage_status probe_time(autosage_plan_s *P, ProbeBufs &pb, int reps, double &
 }
 
 bool same_sched(const Sched &a, const Sched &b) {
-  return a.kind == b.kind && a.G == b.G && a.E == b.E && a.split == b.split && a.pe == b.pe;
+  return a.kind == b.kind && a.G == b.G && a.E == b.E && a.split == b.split && a.pe == b.pe && a.G2 == b.G2;
 }
 
 struct Candidate {
@@ -1044,8 +1049,9 @@ std::vector<Candidate> candidates(const DeviceInfo &dev, const autosage_plan_s *
 // Neighbours of a schedule for the probes' local refinement: half or twice
 // the edge lanes, half or twice the feature lanes, a quarter or four times
 // the chunk length (merge path: the items per warp), the other chunked
-// family (split <-> binned) with the same lanes and chunk length, and for
-// SDDMM the other reduction form (per edge <-> batched). Automatic
+// family (split <-> binned) with the same lanes and chunk length, for
+// SDDMM the other reduction form (per edge <-> batched), and for unfused
+// attention half or twice the aggregation stage's feature lanes. Automatic
 // lanes (0) are first resolved the way the kernels resolve them.
 std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *P, const RowStats &st,
                                   const Sched &b) {
@@ -1066,6 +1072,9 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
     Geom g{};
     if (!cand_geom(P, x.G, x.E, g)) return;
     if (P->op != AUTOSAGE_OP_SDDMM || x.G < 4) x.pe = 0;
+    if (P->op != AUTOSAGE_OP_ATTN_UNFUSED || x.G2 == x.G) x.G2 = 0;
+    Geom ga{};
+    if (x.G2 > 0 && !cand_geom(P, x.G2, x.E, ga)) return;
     if (softmax && x.E != 1) return;
     if (x.kind == AUTOSAGE_SCHED_MERGEPATH) {
       const bool spmm = P->op == AUTOSAGE_OP_SPMM || P->op == AUTOSAGE_OP_SPMM_T;
@@ -1088,19 +1097,25 @@ std::vector<Candidate> neighbours(const DeviceInfo &dev, const autosage_plan_s *
     if (e2 < 1 || e2 > 32) continue;
     // SpMM's merge path keeps whole warps: the feature lanes follow the edge lanes
     const bool whole = b.kind == AUTOSAGE_SCHED_MERGEPATH && P->op != AUTOSAGE_OP_SDDMM;
-    add(Sched{b.kind, whole ? 32 / e2 : G, e2, b.split, b.pe});
+    add(Sched{b.kind, whole ? 32 / e2 : G, e2, b.split, b.pe, b.G2});
   }
   if ((b.kind != AUTOSAGE_SCHED_MERGEPATH || P->op == AUTOSAGE_OP_SDDMM) && !softmax)
     for (int g2 : {G / 2, G * 2})
-      if (g2 >= 1) add(Sched{b.kind, g2, E, b.split, b.pe});
+      if (g2 >= 1) add(Sched{b.kind, g2, E, b.split, b.pe, b.G2});
   if (b.kind != AUTOSAGE_SCHED_ROWGROUP)
-    for (int s2 : {b.split / 4, b.split * 4}) add(Sched{b.kind, G, E, s2, b.pe});
-  if (b.kind == AUTOSAGE_SCHED_SPLIT) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe});
-  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_SPLIT, G, E, b.split, b.pe});
-  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_HYBRID, G, E, b.split, b.pe});
-  if (b.kind == AUTOSAGE_SCHED_HYBRID) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe});
-  if (b.kind == AUTOSAGE_SCHED_ROWGROUP && maxd > 128) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, 128, b.pe});
-  if (P->op == AUTOSAGE_OP_SDDMM) add(Sched{b.kind, G, E, b.split, 1 - b.pe});
+    for (int s2 : {b.split / 4, b.split * 4}) add(Sched{b.kind, G, E, s2, b.pe, b.G2});
+  if (b.kind == AUTOSAGE_SCHED_SPLIT) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe, b.G2});
+  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_SPLIT, G, E, b.split, b.pe, b.G2});
+  if (b.kind == AUTOSAGE_SCHED_BINNED) add(Sched{AUTOSAGE_SCHED_HYBRID, G, E, b.split, b.pe, b.G2});
+  if (b.kind == AUTOSAGE_SCHED_HYBRID) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, b.split, b.pe, b.G2});
+  if (b.kind == AUTOSAGE_SCHED_ROWGROUP && maxd > 128) add(Sched{AUTOSAGE_SCHED_BINNED, G, E, 128, b.pe, b.G2});
+  if (P->op == AUTOSAGE_OP_SDDMM) add(Sched{b.kind, G, E, b.split, 1 - b.pe, b.G2});
+  // unfused attention: half or twice the aggregation stage's feature lanes
+  if (P->op == AUTOSAGE_OP_ATTN_UNFUSED) {
+    const int Ga = b.G2 > 0 ? b.G2 : G;
+    for (int ga : {Ga / 2, Ga * 2})
+      if (ga >= 1 && ga <= 32) add(Sched{b.kind, G, E, b.split, b.pe, ga});
+  }
   return out;
 }
 
@@ -1186,11 +1201,16 @@ autosage_status autosage_plan_with_schedule(const autosage_csr *A, autosage_op o
       sched->lanes_f > 32 || sched->lanes_e > 32 || sched->lanes_f * std::max(1, sched->lanes_e) > 32)
     return fail(AUTOSAGE_ERR_INVALID_ARG, "lanes must be powers of two with lanes_f * lanes_e <= 32");
   if (sched->split < 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "negative split");
+  if (sched->lanes_f_agg && (op != AUTOSAGE_OP_ATTN_UNFUSED || !is_pow2(sched->lanes_f_agg) ||
+                             sched->lanes_f_agg * std::max(1, sched->lanes_e) > 32))
+    return fail(AUTOSAGE_ERR_INVALID_ARG,
+                "lanes_f_agg: unfused attention only, a power of two with lanes_f_agg * lanes_e <= 32");
   cudaStream_t s = as_stream(stream);
   autosage_plan_s *P = nullptr;
   autosage_status st = make_plan_shell(A, op, F, heads, dt, &P, s);
   if (st != AUTOSAGE_OK) return st;
-  P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split, sched->per_edge ? 1 : 0};
+  P->sched = Sched{sched->kind, sched->lanes_f, sched->lanes_e, sched->split, sched->per_edge ? 1 : 0,
+                   sched->lanes_f_agg == sched->lanes_f ? 0 : sched->lanes_f_agg};
   if ((P->sched.kind == AUTOSAGE_SCHED_SPLIT || P->sched.kind == AUTOSAGE_SCHED_BINNED ||
        P->sched.kind == AUTOSAGE_SCHED_HYBRID) && P->sched.split == 0)
     P->sched.split = 1024;
@@ -1373,8 +1393,8 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
       }
       ++ok_count;
       passed.push_back({ms, c});
-      log_line("plan key=%s probe %s G=%d E=%d split=%d pe=%d est_ms=%.4f probe_ms=%.4f", key.c_str(),
-               sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, c.sc.pe, c.est * 1e3, ms);
+      log_line("plan key=%s probe %s G=%d E=%d split=%d pe=%d agg=%d est_ms=%.4f probe_ms=%.4f", key.c_str(),
+               sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, c.sc.pe, c.sc.G2, c.est * 1e3, ms);
       if (best_ms < 0 || ms < best_ms) {
         best_ms = ms;
         best = c.sc;
@@ -1433,8 +1453,8 @@ autosage_status autosage_plan(const autosage_csr *A, autosage_op op, int64_t F, 
         P->sched = c.sc;
         double ms = 0;
         if (build_workspace(P, s) != AUTOSAGE_OK || probe_time(P, pb, 11, ms, s) != AUTOSAGE_OK) continue;
-        log_line("plan key=%s final %s G=%d E=%d split=%d pe=%d probe_ms=%.4f", key.c_str(), sched_name(c.sc.kind),
-                 c.sc.G, c.sc.E, c.sc.split, c.sc.pe, ms);
+        log_line("plan key=%s final %s G=%d E=%d split=%d pe=%d agg=%d probe_ms=%.4f", key.c_str(),
+                 sched_name(c.sc.kind), c.sc.G, c.sc.E, c.sc.split, c.sc.pe, c.sc.G2, ms);
         if (final_ms < 0 || ms < final_ms) {
           final_ms = ms;
           best = c.sc;
@@ -1481,10 +1501,10 @@ autosage_status autosage_plan_destroy(autosage_plan_t plan) {
 autosage_status autosage_plan_describe(autosage_plan_t P, char *buf, size_t len) {
   if (!P || !buf || len == 0) return fail(AUTOSAGE_ERR_INVALID_ARG, "bad describe arguments");
   snprintf(buf, len, "op=%d sched=%s G=%d E=%d split=%d chunks=%d long_rows=%d mp_warps=%" PRId64
-           " probe_ms=%.4f est_ms=%.4f cache=%d per_edge=%d fixed_vals=%d",
+           " probe_ms=%.4f est_ms=%.4f cache=%d per_edge=%d fixed_vals=%d agg_lanes=%d",
            (int)P->op, sched_name(P->sched.kind), P->sched.G, P->sched.E, P->sched.split, P->cl.n_chunks,
            P->cl.n_long, P->mp_warps, P->probe_ms, P->est_ms, P->from_cache ? 1 : 0, P->sched.pe,
-           P->fixed_vals ? 1 : 0);
+           P->fixed_vals ? 1 : 0, P->sched.G2);
   return AUTOSAGE_OK;
 }
 
@@ -1496,6 +1516,7 @@ autosage_status autosage_plan_schedule(autosage_plan_t P, autosage_schedule *sch
     sched->lanes_e = P->sched.E;
     sched->split = P->sched.split;
     sched->per_edge = P->sched.pe;
+    sched->lanes_f_agg = P->sched.G2;
   }
   if (probe_ms) *probe_ms = P->probe_ms;
   return AUTOSAGE_OK;
@@ -1910,10 +1931,13 @@ autosage_status autosage_cache_save(const char *path) {
   {
     std::lock_guard<std::mutex> lk(g_cache_mu);
     fprintf(f, "%s\n", kCacheHeader);
-    for (const auto &kv : g_cache)
-      fprintf(f, "%s\t%s %d %d %d %.6f%s\n", kv.first.c_str(), sched_name(kv.second.sched.kind),
+    for (const auto &kv : g_cache) {
+      fprintf(f, "%s\t%s %d %d %d %.6f%s", kv.first.c_str(), sched_name(kv.second.sched.kind),
               kv.second.sched.G, kv.second.sched.E, kv.second.sched.split, kv.second.probe_ms,
               kv.second.sched.pe ? " edge" : "");
+      if (kv.second.sched.G2 > 0) fprintf(f, " agg=%d", kv.second.sched.G2);
+      fputc('\n', f);
+    }
   }
   const bool ok = fflush(f) == 0;
   fclose(f);
@@ -1945,15 +1969,25 @@ autosage_status autosage_cache_load(const char *path) {
       ++bad;
       continue;
     }
-    // optional marker: per-edge SDDMM reductions
-    std::string rest;
-    if (vs >> rest) {
-      std::string more;
-      if (rest != "edge" || (vs >> more)) {
-        ++bad;
-        continue;
+    // optional markers: per-edge SDDMM reductions ("edge"), the aggregation
+    // stage's feature lanes of unfused attention ("agg=G")
+    std::string tok;
+    bool ok = true;
+    while (ok && vs >> tok) {
+      if (tok == "edge" && !e.sched.pe) {
+        e.sched.pe = 1;
+      } else if (tok.compare(0, 4, "agg=") == 0 && e.sched.G2 == 0) {
+        char *end = nullptr;
+        const long v = strtol(tok.c_str() + 4, &end, 10);
+        ok = end && *end == 0 && v >= 1 && v <= 32 && is_pow2(v);
+        e.sched.G2 = ok ? (int)v : 0;
+      } else {
+        ok = false;
       }
-      e.sched.pe = 1;
+    }
+    if (!ok) {
+      ++bad;
+      continue;
     }
     if (kind == "rowgroup") e.sched.kind = AUTOSAGE_SCHED_ROWGROUP;
     else if (kind == "split") e.sched.kind = AUTOSAGE_SCHED_SPLIT;

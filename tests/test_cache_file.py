@@ -58,6 +58,21 @@ def test_hybrid_schedule_round_trip(tmp_path, sga):
     sga.autosage_cache_clear()
 
 
+def test_aggregation_lanes_marker_round_trip(tmp_path, sga):
+    # unfused attention whose aggregation stage runs with its own feature lanes
+    # carries the optional `agg=G` marker (alone or after `edge`)
+    sga.autosage_cache_clear()
+    line = "NVIDIA_GB300|sm152|op4|dt1|F64|H8|n10|m10|nnz20|fp00000000000000ab\tbinned 16 1 512 5.740000 agg=32\n"
+    p = tmp_path / "c.txt"
+    p.write_text(HEADER + line)
+    sga.autosage_cache_load(str(p))
+    assert sga.autosage_cache_size() == 1
+    q = tmp_path / "d.txt"
+    sga.autosage_cache_save(str(q))
+    assert q.read_text() == HEADER + line
+    sga.autosage_cache_clear()
+
+
 def test_wrong_header_rejected(tmp_path, sga):
     sga.autosage_cache_clear()
     p = tmp_path / "c.txt"
@@ -77,6 +92,10 @@ def test_wrong_header_rejected(tmp_path, sga):
     "key\tsplit 16 4 0 0.1\n",                 # split schedule without a chunk length
     "key\trowgroup 16 4 0 0.1 extra\n",        # trailing field
     "key\trowgroup 16 4 0 0.1 edge edge\n",    # marker twice
+    "key\trowgroup 16 1 0 0.1 agg=24\n",       # aggregation lanes not a power of two
+    "key\trowgroup 16 1 0 0.1 agg=64\n",       # more aggregation lanes than a warp
+    "key\trowgroup 16 1 0 0.1 agg=16x\n",      # not a number
+    "key\trowgroup 16 1 0 0.1 agg=16 agg=32\n",  # marker twice
     "\tsplit 16 2 512 0.1\n",                  # empty key
 ])
 def test_corrupt_lines_are_skipped(tmp_path, sga, bad):

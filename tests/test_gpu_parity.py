@@ -288,6 +288,34 @@ def test_attention_bf16_multihead(skew, fused):
     assert_close(to_np(O), ref, TOL_BF16, f"attention bf16 fused={fused}")
 
 
+# the aggregation stage of unfused attention with its own feature lanes
+# (fewer, more, or the same as the score stage), fp32 and bf16
+@pytest.mark.parametrize("kind,G,E,split,agg", [
+    (sga.SCHED_BINNED, 16, 1, 512, 32), (sga.SCHED_BINNED, 16, 1, 32, 8), (sga.SCHED_ROWGROUP, 8, 2, 0, 16),
+    (sga.SCHED_SPLIT, 16, 2, 16, 8), (sga.SCHED_ROWGROUP, 32, 1, 0, 32),
+], ids=["binned-16-agg32", "binned-16-agg8", "rowgroup-8x2-agg16", "split-16x2-agg8", "rowgroup-32-agg32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unfused_attention_aggregation_lanes(skew, kind, G, E, split, agg, dtype):
+    g = skew
+    A = mat(g)
+    H, D = 8, 64
+    Q = synth.normal(g.n_rows, H * D, 12, synth.STREAM_Q)
+    K = synth.normal(g.n_cols, H * D, 12, synth.STREAM_K)
+    V = synth.normal(g.n_cols, H * D, 12, synth.STREAM_V)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    if dtype == "bf16":
+        (Qd, Q), (Kd, K), (Vd, V) = bf16_tensor(Q), bf16_tensor(K), bf16_tensor(V)
+    else:
+        Qd, Kd, Vd = dev(Q), dev(K), dev(V)
+    plan = sga.autosage_plan_with_schedule(A, sga.OP_ATTN_UNFUSED, D, kind, lanes_f=G, lanes_e=E, split=split,
+                                           heads=H, dtype=tdt, lanes_f_agg=agg)
+    want = 0 if agg == G else agg
+    assert plan.schedule()["lanes_f_agg"] == want and f"agg_lanes={want}" in plan.describe()
+    O = sga.autosage_csr_attention(A, Qd, Kd, Vd, H, 0.125, fused=False, plan=plan)
+    ref = oracle.csr_attention(g.row_ptr, g.col_idx, Q, K, V, H, 0.125)
+    assert_close(to_np(O), ref, TOL_BF16 if dtype == "bf16" else TOL_F32, f"unfused agg lanes {agg} {dtype}")
+
+
 def test_edge_softmax_aggregate_benchmark_shape():
     g = synth.attention_benchmark_shape(0)
     A = mat(g)

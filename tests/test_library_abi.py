@@ -96,6 +96,25 @@ def test_no_alloc_entry_checks_its_csr_on_the_host(lib_path):
     assert lib.autosage_plan_rebind(None, ctypes.byref(ok), None) == sga.ERR_INVALID_ARG
 
 
+def test_aggregation_lanes_are_checked_on_the_host(lib_path):
+    # lanes_f_agg belongs to unfused attention and must be a power of two that
+    # fits a warp with the edge lanes; bad values are refused before the CSR
+    # is touched (the addresses below are never dereferenced)
+    import ctypes
+    import sparse_gnn_aggregation_gb300 as sga
+    lib = sga.library()
+    A = sga._Csr(4, 4, 4, 0x20000, 0x30000, 0)
+    out = ctypes.c_void_p()
+    for op, agg, lanes_e in ((sga.OP_SPMM, 16, 1), (sga.OP_ATTN, 16, 1), (sga.OP_ATTN_UNFUSED, 24, 1),
+                             (sga.OP_ATTN_UNFUSED, 32, 2), (sga.OP_ATTN_UNFUSED, 64, 1)):
+        s = sga._Schedule(sga.SCHED_BINNED, 16, lanes_e, 512, 0, agg)
+        st = lib.autosage_plan_with_schedule(ctypes.byref(A), op, 64, 8, sga.BF16, ctypes.byref(s),
+                                             ctypes.byref(out), None)
+        assert st == sga.ERR_INVALID_ARG, (op, agg, lanes_e)
+        assert b"lanes_f_agg" in lib.autosage_last_error()
+        assert out.value is None
+
+
 def test_header_is_plain_c_and_a_c_program_links(lib_path, tmp_path):
     # the boundary is usable from C: the header compiles as C11 (no C++ or
     # torch types), and a C program links against the library and calls the
