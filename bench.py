@@ -19,6 +19,13 @@ Algorithmic bytes per operation (CSR arrays + gathered rows + outputs):
   unfused attention: the fused bytes + 5 * 4 nnz H (scores written, read
                      twice and written by the softmax, read by the SpMM)
 
+Cache-aware bound: the rates of random 1 KB row gathers from an L2-resident
+table and from one 16x L2 are measured first (autosage_measure_gather). An
+operation needs at least max(DRAM bytes / DRAM gather rate, algorithmic
+bytes / L2 gather rate), with its DRAM bytes from profiles/traffic.txt (an
+ncu count); per_op and roofline report that bound and its fraction of the
+measured time (cache_aware_frac), beside the plain fraction of the HBM peak.
+
 --impl reference times the CPU oracle (fp64, all host cores) on a bounded
 row sample of the same workload and prints the same JSON line with
 "impl": "reference".
@@ -101,12 +108,37 @@ def traffic_for(op_key: str):
     return None
 
 
-def roofline_entry(dom_key, per_op, achieved, peak, peak_src):
+def gather_peaks(dev):
+    """Measured read rates of random 1 KB row gathers on this GPU (the library's
+    autosage_measure_gather): from an L2-resident table (a third of L2), the rate
+    at which L2 serves hot gathered rows, and from a table of 16x L2, the DRAM
+    rate of the same access pattern."""
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    return {"l2_GBps": round(sga.autosage_measure_gather(l2 // 3, 1024, 1 << 24, 5), 1),
+            "dram_GBps": round(sga.autosage_measure_gather(16 * l2, 1024, 1 << 24, 5), 1),
+            "row_bytes": 1024, "table_bytes": [l2 // 3, 16 * l2]}
+
+
+def cache_bound(op_bytes_, traffic, ms, gp):
+    """Cache-aware bound of one operation: every algorithmic byte passes through
+    L2 (at most the L2 gather rate) and the DRAM bytes ncu counted come from HBM
+    (at most the DRAM gather rate), so the operation needs at least the larger
+    of the two times. Returns (bound_ms, bound_ms / ms), or Nones without the
+    DRAM count."""
+    if not traffic or not gp:
+        return None, None
+    t = max(traffic / (gp["dram_GBps"] * 1e6), op_bytes_ / (gp["l2_GBps"] * 1e6))
+    return round(t, 4), round(t / ms, 4)
+
+
+def roofline_entry(dom_key, per_op, achieved, peak, peak_src, gp=None):
     """The dominant operation against the measured HBM peak: `achieved` counts
     algorithmic bytes (L2 hits included); `traffic` is the DRAM bytes of one
     launch from profiles/traffic.txt (null once its kernels changed), and
     traffic_GBps / traffic_frac the DRAM rate those bytes give at the bench's
-    time: what the launch really asks of HBM."""
+    time: what the launch really asks of HBM. With the measured gather rates
+    (gp): l2_frac = achieved / the L2 gather rate, and cache_aware_frac = the
+    cache-aware bound (cache_bound) / the measured time."""
     if not dom_key:
         return {"bound": "hbm", "kernel": None, "achieved": None, "peak": peak, "unit": "GB/s", "frac": None,
                 "traffic": None}
@@ -118,6 +150,11 @@ def roofline_entry(dom_key, per_op, achieved, peak, peak_src):
         gbs = traffic / per_op[dom_key]["ms"] / 1e6
         e["traffic_GBps"] = round(gbs, 1)
         e["traffic_frac"] = round(gbs / peak, 4)
+    if gp:
+        e["gather_peaks"] = gp
+        e["l2_frac"] = round(achieved / gp["l2_GBps"], 4)
+        ms = per_op[dom_key]["ms"]
+        e["cache_aware_bound_ms"], e["cache_aware_frac"] = cache_bound(achieved * ms * 1e6, traffic, ms, gp)
     return e
 
 
@@ -446,6 +483,9 @@ def run_ours(args):
         outs[key] = run(key, kind, gname, F, feats[key])
     torch.cuda.synchronize()
 
+    # the gather-rate ceilings of this GPU (before the timed region)
+    gpeaks = None if args.no_gather_peaks else gather_peaks(dev)
+
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     ev = {key: [] for key, *_ in ops}
@@ -508,6 +548,12 @@ def run_ours(args):
         per_op[key] = {"ms": round(mean_ms, 5), "GBps": round(b / mean_ms / 1e6, 1),
                        "nnzF_per_s": g.nnz * width / (mean_ms * 1e-3),
                        "warm_l2_ms": round(warm_ms, 5), "plan": plans[key].describe()}
+        tr = traffic_for(key)
+        if tr:
+            per_op[key]["dram_GBps"] = round(tr / mean_ms / 1e6, 1)
+        if gpeaks:
+            per_op[key]["l2_frac"] = round(b / mean_ms / 1e6 / gpeaks["l2_GBps"], 4)
+            per_op[key]["cache_aware_bound_ms"], per_op[key]["cache_aware_frac"] = cache_bound(b, tr, mean_ms, gpeaks)
         tot_ms += mean_ms
         tot_bytes += b
         tot_flops += fl
@@ -673,7 +719,7 @@ def run_ours(args):
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "nnzF_per_s": tot_nnzF * world / max(step_ms * 1e-3, 1e-12),
         "edges_per_s": sum(graphs[g].nnz for _, _, g, _ in ops) * world / max(step_ms * 1e-3, 1e-12),
-        "roofline": roofline_entry(dom_key, per_op, achieved, peak, peak_src),
+        "roofline": roofline_entry(dom_key, per_op, achieved, peak, peak_src, gpeaks),
         "clocks": clock_info,
         "gpu_launches": n_launch,
         "plan_seconds": round(plan_s, 2),
@@ -840,6 +886,8 @@ def main():
     ap.add_argument("--no-next", action="store_true", help="skip the rows measured beyond the step")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the products-like and Reddit-like throughput rows")
+    ap.add_argument("--no-gather-peaks", action="store_true",
+                    help="skip measuring the L2 and DRAM gather rates (the cache-aware bound)")
     ap.add_argument("--only", default=None, help="run only operations whose key contains one of these comma-separated texts "
                          "(backward, typed: the rows measured beyond the step)")
     ap.add_argument("--scale", type=int, default=20, help="R-MAT scale (20 is the benchmark workload)")

@@ -40,7 +40,7 @@ EXPORTS = [
     "autosage_status_string", "autosage_last_error", "autosage_version",
     "autosage_csr_attention_unfused_noalloc", "autosage_csr_attention_backward",
     "autosage_plan_typed", "autosage_spmm_typed", "autosage_plan_rebind",
-    "autosage_partition_rows", "autosage_shard_halo", "autosage_gather_rows",
+    "autosage_partition_rows", "autosage_shard_halo", "autosage_gather_rows", "autosage_measure_gather",
 ]
 
 
@@ -93,6 +93,7 @@ def _load():
         "autosage_partition_rows": [P, I64, I, P],
         "autosage_shard_halo": [P, P, I64, I64, I64, P, P, P],
         "autosage_gather_rows": [P, I64, P, I64, I64, I, P, I64, P],
+        "autosage_measure_gather": [I64, I, I64, I, ctypes.POINTER(ctypes.c_double), P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -493,6 +494,17 @@ def autosage_gather_rows(X, idx, out=None, stream=None):
     _check(_lib.autosage_gather_rows(_ptr(X), _ld(X), _ptr(idx), int(idx.numel()), F, _dt(X), _ptr(out), _ld(out),
                                      _stream(stream)))
     return out
+
+
+def autosage_measure_gather(table_bytes: int, row_bytes: int = 1024, n_gathers: int = 1 << 24, reps: int = 5,
+                            stream=None) -> float:
+    """Read rate (GB/s) of random row gathers from a table of table_bytes on the
+    current GPU: L2-resident tables give the L2 rate for hot rows, large ones
+    the DRAM rate. Synchronises the stream."""
+    g = ctypes.c_double()
+    _check(_lib.autosage_measure_gather(int(table_bytes), int(row_bytes), int(n_gathers), int(reps), ctypes.byref(g),
+                                        _stream(stream)))
+    return g.value
 
 
 def autosage_cache_load(path: str):

@@ -387,6 +387,34 @@ __global__ void fill_probe_kernel(void *__restrict__ p, int64_t n, int bf16, uns
   }
 }
 
+// Row indices of the gather-rate measurement: idx[k] = a SplitMix64 hash of
+// k, reduced to [0, rows).
+__global__ void gather_rate_index_kernel(int32_t *__restrict__ idx, int64_t n, int64_t rows,
+                                         unsigned long long seed) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride)
+    idx[k] = (int32_t)(splitmix64_mix(seed + 0x9E3779B97F4A7C15ull * (unsigned long long)(k + 1)) %
+                       (unsigned long long)rows);
+}
+
+// One warp per gathered row of `words` 16-byte words; the loaded words are
+// folded into one value per lane, stored only if it hits a sentinel, so the
+// loads stay and nothing is written.
+__global__ void gather_rate_kernel(const uint4 *__restrict__ table, const int32_t *__restrict__ idx, int64_t n,
+                                   int words, unsigned *__restrict__ sink) {
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int lane = threadIdx.x & 31;
+  unsigned acc = 0;
+  for (int64_t k = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); k < n; k += warps) {
+    const uint4 *row = table + (int64_t)__ldg(idx + k) * words;
+    for (int w = lane; w < words; w += 32) {
+      const uint4 v = __ldg(row + w);
+      acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+  }
+  if (acc == 0x9E3779B9u) *sink = acc;
+}
+
 __global__ void compare_kernel(const void *__restrict__ a, const void *__restrict__ b, int64_t n,
                                int bf16, float rtol, float atol, unsigned long long *__restrict__ count) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -606,6 +634,19 @@ cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const i
 cudaError_t fill_probe(void *p, int64_t n_elems, DType dt, uint64_t seed, cudaStream_t s) {
   if (n_elems <= 0) return cudaSuccess;
   fill_probe_kernel<<<grid_for(n_elems, 256), 256, 0, s>>>(p, n_elems, dt == DType::BF16, seed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rate_index(int32_t *idx, int64_t n, int64_t rows, uint64_t seed, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  gather_rate_index_kernel<<<grid_for(n, 256), 256, 0, s>>>(idx, n, rows, seed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rate(const void *table, const int32_t *idx, int64_t n, int row_bytes, int grid,
+                               unsigned *sink, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  gather_rate_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(table), idx, n, row_bytes / 16, sink);
   return cudaGetLastError();
 }
 

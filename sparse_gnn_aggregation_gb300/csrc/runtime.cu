@@ -1898,6 +1898,59 @@ autosage_status autosage_validate_csr(const autosage_csr *A, void *stream) {
   return AUTOSAGE_OK;
 }
 
+autosage_status autosage_measure_gather(int64_t table_bytes, int row_bytes, int64_t n_gathers, int reps,
+                                        double *gbps, void *stream) {
+  if (!gbps) return fail(AUTOSAGE_ERR_INVALID_ARG, "gbps is NULL");
+  *gbps = 0;
+  if (row_bytes < 16 || row_bytes > 4096 || row_bytes % 16)
+    return fail(AUTOSAGE_ERR_INVALID_ARG, "row_bytes must be a multiple of 16 in [16, 4096]");
+  if (table_bytes < row_bytes) return fail(AUTOSAGE_ERR_INVALID_ARG, "the table must hold at least one row");
+  if (n_gathers < 1 || n_gathers >= INT32_MAX) return fail(AUTOSAGE_ERR_INVALID_ARG, "n_gathers out of range");
+  if (reps < 1 || reps > 1000) return fail(AUTOSAGE_ERR_INVALID_ARG, "reps must be in [1, 1000]");
+  const int64_t rows = table_bytes / row_bytes;
+  if (rows >= INT32_MAX) return fail(AUTOSAGE_ERR_UNSUPPORTED, "more table rows than int32 indices address");
+  cudaStream_t s = as_stream(stream);
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int grid = sms * 4;  // four 256-thread blocks per SM: the fastest of 4 and 8 measured
+  void *table = nullptr, *sink = nullptr;
+  int32_t *idx = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  float best = -1.f;
+  cudaError_t e = cudaMallocAsync(&table, (size_t)(rows * row_bytes), s);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void **>(&idx), sizeof(int32_t) * (size_t)n_gathers, s);
+  if (e == cudaSuccess) e = cudaMallocAsync(&sink, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(table, 0x5a, (size_t)(rows * row_bytes), s);
+  if (e == cudaSuccess) e = launch_gather_rate_index(idx, n_gathers, rows, 0x5EEDull, s);
+  if (e == cudaSuccess) e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  // one untimed run, then `reps` timed runs; the fastest is the rate
+  if (e == cudaSuccess)
+    e = launch_gather_rate(table, idx, n_gathers, row_bytes, grid, static_cast<unsigned *>(sink), s);
+  for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+    e = cudaEventRecord(e0, s);
+    if (e == cudaSuccess)
+      e = launch_gather_rate(table, idx, n_gathers, row_bytes, grid, static_cast<unsigned *>(sink), s);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    if (e == cudaSuccess && ms > 0.f && (best < 0.f || ms < best)) best = ms;
+  }
+  if (table) cudaFreeAsync(table, s);
+  if (idx) cudaFreeAsync(idx, s);
+  if (sink) cudaFreeAsync(sink, s);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  const cudaError_t es = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = es;
+  if (e != cudaSuccess) return cuda_fail(e, "gather rate");
+  if (best <= 0.f) return fail(AUTOSAGE_ERR_CUDA, "gather rate: no timed run");
+  *gbps = (double)n_gathers * row_bytes / (best * 1e-3) / 1e9;
+  return AUTOSAGE_OK;
+}
+
 autosage_status autosage_csr_transpose(const autosage_csr *A, int32_t *row_ptr_t, int32_t *col_idx_t,
                                        float *vals_t, void *stream) {
   autosage_status st = check_csr(A, true);

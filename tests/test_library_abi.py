@@ -96,6 +96,19 @@ def test_no_alloc_entry_checks_its_csr_on_the_host(lib_path):
     assert lib.autosage_plan_rebind(None, ctypes.byref(ok), None) == sga.ERR_INVALID_ARG
 
 
+def test_gather_rate_arguments_are_checked_on_the_host(lib_path):
+    # bad sizes are refused before any device call (no GPU here)
+    import ctypes
+    import sparse_gnn_aggregation_gb300 as sga
+    lib = sga.library()
+    g = ctypes.c_double(-1.0)
+    for table, row, n, reps in ((1 << 20, 8, 100, 1), (1 << 20, 4112, 10, 1), (1 << 20, 1000, 10, 1),
+                                (100, 1024, 10, 1), (1 << 20, 1024, 0, 1), (1 << 20, 1024, 10, 0)):
+        assert lib.autosage_measure_gather(table, row, n, reps, ctypes.byref(g), None) == sga.ERR_INVALID_ARG
+        assert g.value == 0.0
+    assert lib.autosage_measure_gather(1 << 20, 1024, 10, 1, None, None) == sga.ERR_INVALID_ARG
+
+
 def test_aggregation_lanes_are_checked_on_the_host(lib_path):
     # lanes_f_agg belongs to unfused attention and must be a power of two that
     # fits a warp with the edge lanes; bad values are refused before the CSR
