@@ -65,13 +65,14 @@ cudaError_t launch_attention(const Geom &g, int64_t n_rows, const int32_t *row_p
 
 // Merge-path SpMM: warp w covers diagonals [w*items, (w+1)*items) of the
 // (rows + edges) merge path; part: [n_warps + 1] int2 (row, edge) starts.
+// Shares of at most 256 items are staged in shared memory first.
 // carry_val: [n_warps * F] fp32 (the row left unfinished at a warp's end),
 // carry_row: [n_warps] int32, head_val: [n_warps * F] fp32 (the last segment
 // of a row that earlier warps began, added and rounded by the fix-up).
 cudaError_t launch_spmm_mergepath(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                                   const int32_t *col_idx, const float *vals, const void *X,
                                   int64_t ldx, void *Y, int64_t ldy, const int2 *part,
-                                  int64_t n_warps, float *carry_val, int32_t *carry_row,
+                                  int64_t n_warps, int items, float *carry_val, int32_t *carry_row,
                                   float *head_val, cudaStream_t s);
 cudaError_t launch_mergepath_partition(int64_t n_rows, int64_t nnz, const int32_t *row_ptr,
                                        int64_t items, int64_t n_warps, int2 *part, cudaStream_t s);

@@ -594,7 +594,7 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
         if (mp) {
           gt.E = 32 / gt.G;
           e = launch_spmm_mergepath(gt, wk.rows, wk.row_ptr, wk.col_idx, wk.vals, x, a.ldx, y,
-                                    a.ldy, P->mp_part.as<int2>(), P->mp_warps, P->mp_carry_val.as<float>(),
+                                    a.ldy, P->mp_part.as<int2>(), P->mp_warps, P->sched.split, P->mp_carry_val.as<float>(),
                                     P->mp_carry_row.as<int32_t>(), P->mp_head_val.as<float>(), s);
         } else {
           e = launch_spmm(gt, wk.rows, wk.row_ptr, wk.col_idx, wk.vals, x, a.ldx, y, a.ldy, cl,

@@ -113,6 +113,40 @@ __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx
   }
 }
 
+// gather_edges over column indices and weights staged in shared memory (sc,
+// sv: entries for the edges from `base` on; sv null: weight 1): the same
+// rounds and the same order of additions, with the index and weight loads
+// served from shared memory instead of global memory.
+template <typename T, int VW, int NV, int U, bool COMP>
+__device__ __forceinline__ void gather_staged(const int32_t *sc, const float *sv, int base, const T *__restrict__ X,
+                                              int64_t ldx, int nfrag, const int (&frag)[NV], int E, int p0, int pe,
+                                              float (&acc)[NV][VW], float (&comp)[NV][VW]) {
+  for (int p = p0; p < pe; p += U * E) {
+    int c[U];
+    float w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = p + u * E;
+      c[u] = q < pe ? sc[q - base] : 0;
+      w[u] = (q < pe && sv) ? sv[q - base] : 1.f;
+    }
+    Frag<T, VW> f[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (p + u * E < pe && frag[k] < nfrag) f[u][k].load(X + (int64_t)c[u] * ldx + (int64_t)frag[k] * VW);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (p + u * E < pe)
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (frag[k] < nfrag)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) accum<COMP>(acc[k][v], comp[k][v], w[u], f[u][k].get(v));
+  }
+}
+
 // Sum the E edge-lane partials of a group (xor butterfly, fixed order).
 template <int NV, int VW>
 __device__ __forceinline__ void reduce_edge_lanes(float (&acc)[NV][VW], unsigned mask, int G, int GE) {
@@ -222,8 +256,28 @@ __global__ void mergepath_partition_kernel(int64_t n_rows, int64_t nnz,
   part[w] = merge_path_search(d, n_rows, nnz, row_ptr);
 }
 
-template <typename T, int VW, int NV, bool COMP>
-__global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
+// Edges of one warp's share that the staged merge path keeps in shared
+// memory (with their weights and the share's row bounds): shares of at most
+// this many items are staged.
+constexpr int kStageItems = 256;
+
+// STAGED: the warp first copies its share's column indices, weights and row
+// bounds into shared memory with coalesced loads (one memory round trip for
+// the share), so no row waits on its own index loads; the gathers and the
+// order of additions are those of the plain form.
+// Blocks per SM the staged form's register budget is sized for: lanes of up
+// to 4 elements run four 256-thread blocks (64 registers), lanes of 8 three
+// (80 registers; at 85 the allocation rounds up and only two fit: R-MAT
+// F = 256 ran 1.84 ms against 1.49 ms at three blocks, F = 64 0.57 ms at
+// three blocks against 0.52 ms at four). Lanes of more than 4 fragments
+// (single-element fragments of unaligned rows) spilled at those bounds.
+template <int VW, int NV, bool STAGED>
+constexpr int mp_min_blocks() {
+  return (!STAGED || NV > 4) ? 1 : (NV * VW <= 4 ? 4 : (NV * VW <= 8 ? 3 : 1));
+}
+
+template <typename T, int VW, int NV, bool COMP, bool STAGED>
+__global__ void __launch_bounds__(kBlock, mp_min_blocks<VW, NV, STAGED>()) spmm_mergepath_kernel(
     int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
     const float *__restrict__ vals, const T *__restrict__ X, int64_t ldx, T *__restrict__ Y,
     int64_t ldy, int nfrag, int G, int E, const int2 *__restrict__ part, int64_t n_warps,
@@ -237,16 +291,42 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
 #pragma unroll
   for (int k = 0; k < NV; ++k) frag[k] = L.g + k * G;
   constexpr int U = unroll_for<NV, VW>();
+  // the share's row bounds (rp[j] = row_ptr[s0.x + j], j <= rows of the share),
+  // column indices and weights
+  const int32_t *rp = row_ptr + s0.x;
+  const int32_t *sc = nullptr;
+  const float *sv = nullptr;
+  if constexpr (STAGED) {
+    __shared__ int32_t s_rp[kBlock / 32][kStageItems + 1];
+    __shared__ int32_t s_col[kBlock / 32][kStageItems];
+    __shared__ float s_val[kBlock / 32][kStageItems];
+    const int wl = threadIdx.x >> 5;
+    const int nr = s1.x - s0.x, ne = s1.y - s0.y;  // nr + ne <= items <= kStageItems
+    for (int j = L.lane; j <= nr; j += 32) s_rp[wl][j] = __ldg(row_ptr + s0.x + j);
+    for (int j = L.lane; j < ne; j += 32) s_col[wl][j] = ld_stream_i32(col_idx + s0.y + j);
+    if (vals)
+      for (int j = L.lane; j < ne; j += 32) s_val[wl][j] = ld_stream_f32(vals + s0.y + j);
+    __syncwarp();
+    rp = s_rp[wl];
+    sc = s_col[wl];
+    sv = vals ? s_val[wl] : nullptr;
+  }
+  auto gather = [&](int p0, int pe, float (&acc)[NV][VW], float (&comp)[NV][VW]) {
+    if constexpr (STAGED)
+      gather_staged<T, VW, NV, U, COMP>(sc, sv, s0.y, X, ldx, nfrag, frag, E, p0, pe, acc, comp);
+    else
+      gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, true, head, X, ldx, nfrag, frag, E, p0, pe, acc,
+                                       comp);
+  };
   for (int i = s0.x; i < s1.x; ++i) {
-    const int b = max(row_ptr[i], s0.y), e = row_ptr[i + 1];
+    const int b = max(rp[i - s0.x], s0.y), e = rp[i + 1 - s0.x];
     float acc[NV][VW], comp[NV][VW];
     zero(acc);
     zero(comp);
-    gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, true, head, X, ldx, nfrag, frag, E, b + L.e, e, acc,
-                                     comp);
+    gather(b + L.e, e, acc, comp);
     reduce_edge_lanes(acc, FULL, G, 32);
     if (L.e != 0) continue;
-    if (i == s0.x && row_ptr[i] < s0.y) {
+    if (i == s0.x && rp[0] < s0.y) {
       // the last segment of a row that earlier warps began: kept in fp32 for
       // the fix-up, which adds the carries and rounds the row once
       float *hv = head_val + w * (int64_t)nfrag * VW;
@@ -263,14 +343,13 @@ __global__ void __launch_bounds__(kBlock) spmm_mergepath_kernel(
   // the row left unfinished at the warp's end becomes a carry-out
   int crow = -1;
   if (s1.x < n_rows) {
-    const int b = max(row_ptr[s1.x], s0.y);
+    const int b = max(rp[s1.x - s0.x], s0.y);
     if (s1.y > b) {
       crow = s1.x;
       float acc[NV][VW], comp[NV][VW];
       zero(acc);
       zero(comp);
-      gather_edges<T, VW, NV, U, COMP>(col_idx, vals, 1, 1, true, head, X, ldx, nfrag, frag, E, b + L.e, s1.y,
-                                       acc, comp);
+      gather(b + L.e, s1.y, acc, comp);
       reduce_edge_lanes(acc, FULL, G, 32);
       if (L.e == 0) {
         float *cv = carry_val + w * (int64_t)nfrag * VW;
@@ -435,17 +514,23 @@ cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const
 template <typename T, int VW>
 cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const float *vals, const T *X, int64_t ldx, T *Y,
-                         int64_t ldy, const int2 *part, int64_t n_warps, float *carry_val,
+                         int64_t ldy, const int2 *part, int64_t n_warps, int items, float *carry_val,
                          int32_t *carry_row, float *head_val, cudaStream_t s) {
   if (n_warps <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_warps + kBlock / 32 - 1) / (kBlock / 32));
-#define AUTOSAGE_MP_K(NVV, CMP)                                                                    \
-  spmm_mergepath_kernel<T, VW, NVV, CMP><<<grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, vals, X,  \
-                                                                ldx, Y, ldy, g.nfrag, g.G, g.E,     \
-                                                                part, n_warps, carry_val, carry_row, head_val)
-#define AUTOSAGE_MP_NV(NVV)           \
-  if (g.comp) AUTOSAGE_MP_K(NVV, true); \
-  else AUTOSAGE_MP_K(NVV, false);
+  const bool staged = items <= kStageItems;
+#define AUTOSAGE_MP_K(NVV, CMP, STG)                                                                    \
+  spmm_mergepath_kernel<T, VW, NVV, CMP, STG><<<grid, kBlock, 0, s>>>(n_rows, row_ptr, col_idx, vals, X,  \
+                                                                     ldx, Y, ldy, g.nfrag, g.G, g.E,     \
+                                                                     part, n_warps, carry_val, carry_row, head_val)
+#define AUTOSAGE_MP_NV(NVV)                                     \
+  if (g.comp) {                                                 \
+    if (staged) AUTOSAGE_MP_K(NVV, true, true);                 \
+    else AUTOSAGE_MP_K(NVV, true, false);                       \
+  } else {                                                      \
+    if (staged) AUTOSAGE_MP_K(NVV, false, true);                \
+    else AUTOSAGE_MP_K(NVV, false, false);                      \
+  }
   switch (g.NV) {
     case 1: AUTOSAGE_MP_NV(1); break;
     case 2: AUTOSAGE_MP_NV(2); break;
@@ -524,25 +609,25 @@ cudaError_t launch_mergepath_partition(int64_t n_rows, int64_t nnz, const int32_
 cudaError_t launch_spmm_mergepath(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                                   const int32_t *col_idx, const float *vals, const void *X,
                                   int64_t ldx, void *Y, int64_t ldy, const int2 *part,
-                                  int64_t n_warps, float *carry_val, int32_t *carry_row,
+                                  int64_t n_warps, int items, float *carry_val, int32_t *carry_row,
                                   float *head_val, cudaStream_t s) {
   if (g.G * g.E != 32) return cudaErrorInvalidValue;
   if (g.dt == DType::F32) {
     auto x = static_cast<const float *>(X);
     auto y = static_cast<float *>(Y);
     switch (g.VW) {
-      case 4: return mergepath_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
-      case 2: return mergepath_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
-      case 1: return mergepath_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 4: return mergepath_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
+      case 2: return mergepath_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
+      case 1: return mergepath_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
     }
   } else {
     auto x = static_cast<const __nv_bfloat16 *>(X);
     auto y = static_cast<__nv_bfloat16 *>(Y);
     switch (g.VW) {
-      case 8: return mergepath_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
-      case 4: return mergepath_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
-      case 2: return mergepath_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
-      case 1: return mergepath_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, carry_val, carry_row, head_val, s);
+      case 8: return mergepath_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
+      case 4: return mergepath_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
+      case 2: return mergepath_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
+      case 1: return mergepath_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals, x, ldx, y, ldy, part, n_warps, items, carry_val, carry_row, head_val, s);
     }
   }
   return cudaErrorInvalidValue;
