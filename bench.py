@@ -19,7 +19,7 @@ Algorithmic bytes per operation (CSR arrays + gathered rows + outputs):
   unfused attention: the fused bytes + 5 * 4 nnz H (scores written, read
                      twice and written by the softmax, read by the SpMM)
 
-Cache-aware bound: the rates of random 1 KB row gathers from an L2-resident
+Cache-aware bound: the rates of random 2 KB row gathers from an L2-resident
 table and from one 16x L2 are measured first (autosage_measure_gather). An
 operation needs at least max(DRAM bytes / DRAM gather rate, algorithmic
 bytes / L2 gather rate), with its DRAM bytes from profiles/traffic.txt (an
@@ -109,14 +109,19 @@ def traffic_for(op_key: str):
 
 
 def gather_peaks(dev):
-    """Measured read rates of random 1 KB row gathers on this GPU (the library's
+    """Measured read rates of random row gathers on this GPU (the library's
     autosage_measure_gather): from an L2-resident table (a third of L2), the rate
     at which L2 serves hot gathered rows, and from a table of 16x L2, the DRAM
-    rate of the same access pattern."""
+    rate of the same access pattern. Rows of 2 KB (one warp each): the
+    fastest row size measured (1 KB rows: 15.6 and 6.1 TB/s, 2 KB: 19.4 and
+    7.2 TB/s on a GB300), so the rates are ceilings for the 1 KB rows of the
+    widest operations."""
+    import torch
+    import sparse_gnn_aggregation_gb300 as sga
     l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
-    return {"l2_GBps": round(sga.autosage_measure_gather(l2 // 3, 1024, 1 << 24, 5), 1),
-            "dram_GBps": round(sga.autosage_measure_gather(16 * l2, 1024, 1 << 24, 5), 1),
-            "row_bytes": 1024, "table_bytes": [l2 // 3, 16 * l2]}
+    return {"l2_GBps": round(sga.autosage_measure_gather(l2 // 3, 2048, 1 << 23, 5), 1),
+            "dram_GBps": round(sga.autosage_measure_gather(16 * l2, 2048, 1 << 23, 5), 1),
+            "row_bytes": 2048, "table_bytes": [l2 // 3, 16 * l2]}
 
 
 def cache_bound(op_bytes_, traffic, ms, gp):

@@ -353,13 +353,13 @@ autosage_status autosage_csr_transpose(const autosage_csr *A, int32_t *row_ptr_t
 /* Read rate of random row gathers on this GPU: the ceiling a gather kernel meets when its
  * rows come from a table of table_bytes. A table that fits in L2 gives the rate at which L2
  * serves repeatedly gathered (hot) rows; one far larger than L2 gives the DRAM rate. One warp
- * per gathered row reads row_bytes (a multiple of 16 in [16, 4096]) in 16-byte words; each
- * run reads n_gathers rows of the table chosen by a SplitMix64 hash of the gather index.
- * *gbps (HOST) receives n_gathers * row_bytes / the fastest of `reps` timed runs (after one
- * untimed run), in GB/s. Allocates (stream-ordered) a table of table_bytes rounded down to
- * whole rows plus 4 * n_gathers bytes of indices, and frees them before returning.
- * SYNCHRONISES `stream`. Argument errors return AUTOSAGE_ERR_INVALID_ARG before any device
- * call. */
+ * per gathered row reads row_bytes (a multiple of 16 in [16, 4096]) in 16-byte words, all of
+ * a lane's words in flight together; each run reads n_gathers rows of the table, row k chosen
+ * by a SplitMix64 hash of (run, k) computed in the kernel (no index array is read). *gbps
+ * (HOST) receives n_gathers * row_bytes / the fastest of `reps` timed runs (after one untimed
+ * run), in GB/s. Allocates (stream-ordered) a table of table_bytes rounded down to whole rows,
+ * and frees it before returning. SYNCHRONISES `stream`. Argument errors return
+ * AUTOSAGE_ERR_INVALID_ARG before any device call. */
 autosage_status autosage_measure_gather(int64_t table_bytes, int row_bytes, int64_t n_gathers, int reps,
                                         double *gbps, void *stream);
 

@@ -387,30 +387,30 @@ __global__ void fill_probe_kernel(void *__restrict__ p, int64_t n, int bf16, uns
   }
 }
 
-// Row indices of the gather-rate measurement: idx[k] = a SplitMix64 hash of
-// k, reduced to [0, rows).
-__global__ void gather_rate_index_kernel(int32_t *__restrict__ idx, int64_t n, int64_t rows,
-                                         unsigned long long seed) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride)
-    idx[k] = (int32_t)(splitmix64_mix(seed + 0x9E3779B97F4A7C15ull * (unsigned long long)(k + 1)) %
-                       (unsigned long long)rows);
-}
-
-// One warp per gathered row of `words` 16-byte words; the loaded words are
-// folded into one value per lane, stored only if it hits a sentinel, so the
-// loads stay and nothing is written.
-__global__ void gather_rate_kernel(const uint4 *__restrict__ table, const int32_t *__restrict__ idx, int64_t n,
-                                   int words, unsigned *__restrict__ sink) {
+// Gather-rate measurement: gathered row k of a run is a SplitMix64 hash of
+// (seed, k), reduced to [0, rows) by a multiply-high (no index array is read,
+// so only the table's rows move). One warp per gathered row of `words`
+// 16-byte words, S = ceil(words / 32) words a lane: a lane issues all its
+// loads of the row before it uses any, so they are in flight together; the
+// loaded words are folded into one value per lane, stored only if it hits a
+// sentinel, so the loads stay and nothing is written.
+template <int S>
+__global__ void gather_rate_kernel(const uint4 *__restrict__ table, uint32_t rows, int64_t n, int words,
+                                   unsigned long long seed, unsigned *__restrict__ sink) {
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   const int lane = threadIdx.x & 31;
   unsigned acc = 0;
   for (int64_t k = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); k < n; k += warps) {
-    const uint4 *row = table + (int64_t)__ldg(idx + k) * words;
-    for (int w = lane; w < words; w += 32) {
-      const uint4 v = __ldg(row + w);
-      acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    const uint32_t h = (uint32_t)(splitmix64_mix(seed + 0x9E3779B97F4A7C15ull * (unsigned long long)(k + 1)) >> 32);
+    const uint4 *row = table + (int64_t)__umulhi(h, rows) * words;
+    uint4 v[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const int w = lane + 32 * j;
+      v[j] = w < words ? __ldg(row + w) : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int j = 0; j < S; ++j) acc ^= v[j].x ^ v[j].y ^ v[j].z ^ v[j].w;
   }
   if (acc == 0x9E3779B9u) *sink = acc;
 }
@@ -637,16 +637,19 @@ cudaError_t fill_probe(void *p, int64_t n_elems, DType dt, uint64_t seed, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rate_index(int32_t *idx, int64_t n, int64_t rows, uint64_t seed, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  gather_rate_index_kernel<<<grid_for(n, 256), 256, 0, s>>>(idx, n, rows, seed);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gather_rate(const void *table, const int32_t *idx, int64_t n, int row_bytes, int grid,
-                               unsigned *sink, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  gather_rate_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(table), idx, n, row_bytes / 16, sink);
+cudaError_t launch_gather_rate(const void *table, int64_t rows, int64_t n, int row_bytes, int grid,
+                               uint64_t seed, unsigned *sink, cudaStream_t s) {
+  if (n <= 0 || rows <= 0) return cudaSuccess;
+  const uint4 *t = static_cast<const uint4 *>(table);
+  const int words = row_bytes / 16;
+  const uint32_t r = (uint32_t)rows;
+  switch ((words + 31) / 32) {
+    case 1: gather_rate_kernel<1><<<grid, 256, 0, s>>>(t, r, n, words, seed, sink); break;
+    case 2: gather_rate_kernel<2><<<grid, 256, 0, s>>>(t, r, n, words, seed, sink); break;
+    case 3:
+    case 4: gather_rate_kernel<4><<<grid, 256, 0, s>>>(t, r, n, words, seed, sink); break;
+    default: gather_rate_kernel<8><<<grid, 256, 0, s>>>(t, r, n, words, seed, sink); break;
+  }
   return cudaGetLastError();
 }
 

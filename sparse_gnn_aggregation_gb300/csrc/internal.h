@@ -140,11 +140,11 @@ cudaError_t launch_typed_index(int64_t nnz, int64_t n_cols, int n_types, const i
                                const int32_t *edge_type, int32_t *combined, int *err, cudaStream_t s);
 // Deterministic pseudo-random fill of probe buffers (values in [-1, 1)).
 cudaError_t fill_probe(void *p, int64_t n_elems, DType dt, uint64_t seed, cudaStream_t s);
-// Gather-rate measurement: idx[k] in [0, rows) from a hash of k; then one
-// warp per idx entry reads row idx[k] (row_bytes, a multiple of 16) of table.
-cudaError_t launch_gather_rate_index(int32_t *idx, int64_t n, int64_t rows, uint64_t seed, cudaStream_t s);
-cudaError_t launch_gather_rate(const void *table, const int32_t *idx, int64_t n, int row_bytes, int grid,
-                               unsigned *sink, cudaStream_t s);
+// Gather-rate measurement: n rows of `table` (rows rows of row_bytes, a
+// multiple of 16 up to 4096) read by one warp each, row k chosen by a hash of
+// (seed, k).
+cudaError_t launch_gather_rate(const void *table, int64_t rows, int64_t n, int row_bytes, int grid,
+                               uint64_t seed, unsigned *sink, cudaStream_t s);
 // Count elements with |a - b| > atol + rtol * |b| (fp32 or bf16 arrays) into *count (device).
 cudaError_t launch_compare(const void *a, const void *b, int64_t n, DType dt, float rtol,
                            float atol, unsigned long long *count, cudaStream_t s);

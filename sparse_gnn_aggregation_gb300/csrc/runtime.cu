@@ -1915,23 +1915,21 @@ autosage_status autosage_measure_gather(int64_t table_bytes, int row_bytes, int6
   CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int grid = sms * 4;  // four 256-thread blocks per SM: the fastest of 4 and 8 measured
   void *table = nullptr, *sink = nullptr;
-  int32_t *idx = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   float best = -1.f;
   cudaError_t e = cudaMallocAsync(&table, (size_t)(rows * row_bytes), s);
-  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void **>(&idx), sizeof(int32_t) * (size_t)n_gathers, s);
   if (e == cudaSuccess) e = cudaMallocAsync(&sink, sizeof(unsigned), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(table, 0x5a, (size_t)(rows * row_bytes), s);
-  if (e == cudaSuccess) e = launch_gather_rate_index(idx, n_gathers, rows, 0x5EEDull, s);
   if (e == cudaSuccess) e = cudaEventCreate(&e0);
   if (e == cudaSuccess) e = cudaEventCreate(&e1);
-  // one untimed run, then `reps` timed runs; the fastest is the rate
+  // one untimed run, then `reps` timed runs (each its own rows); the fastest is the rate
   if (e == cudaSuccess)
-    e = launch_gather_rate(table, idx, n_gathers, row_bytes, grid, static_cast<unsigned *>(sink), s);
+    e = launch_gather_rate(table, rows, n_gathers, row_bytes, grid, 0x5EEDull, static_cast<unsigned *>(sink), s);
   for (int r = 0; r < reps && e == cudaSuccess; ++r) {
     e = cudaEventRecord(e0, s);
     if (e == cudaSuccess)
-      e = launch_gather_rate(table, idx, n_gathers, row_bytes, grid, static_cast<unsigned *>(sink), s);
+      e = launch_gather_rate(table, rows, n_gathers, row_bytes, grid, 0x5EEDull + 0x1000ull * (r + 1),
+                             static_cast<unsigned *>(sink), s);
     if (e == cudaSuccess) e = cudaEventRecord(e1, s);
     if (e == cudaSuccess) e = cudaEventSynchronize(e1);
     float ms = 0.f;
@@ -1939,7 +1937,6 @@ autosage_status autosage_measure_gather(int64_t table_bytes, int row_bytes, int6
     if (e == cudaSuccess && ms > 0.f && (best < 0.f || ms < best)) best = ms;
   }
   if (table) cudaFreeAsync(table, s);
-  if (idx) cudaFreeAsync(idx, s);
   if (sink) cudaFreeAsync(sink, s);
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
