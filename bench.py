@@ -694,15 +694,25 @@ def run_ours(args):
 
     # launches inside the timed region (per step, our kernels only)
     def launches(key, kind):
+        # SDDMM: one launch (every edge's score is finished in its own item);
+        # SpMM: merge path + its fix-up, or the row kernel, a fix-up for cut rows
+        # and (hybrid) the ELL slab's kernel; fused attention: the row kernel and
+        # a fix-up for cut rows; unfused: SDDMM, the row softmax (with a merge and
+        # a normalisation pass for cut rows) and the SpMM
         d = plans[key].describe()
-        chunks = int(d.split("chunks=")[1].split()[0]) if "chunks=" in d else 0
         long_rows = int(d.split("long_rows=")[1].split()[0]) if "long_rows=" in d else 0
-        mp = "sched=mergepath" in d
-        base = 2 if mp else 1 + (1 if long_rows > 0 else 0)
+        cut = 1 if long_rows > 0 else 0
+        if kind == "sddmm":
+            return 1
+        if "sched=mergepath" in d:
+            spmm = 2
+        else:
+            spmm = 1 + cut + (1 if "sched=hybrid" in d else 0)
+        if kind == "attn_fused":
+            return 1 + cut
         if kind == "attn_unfused":
-            sm = 1 + (3 if long_rows > 0 else 0)
-            return base + sm + base
-        return base
+            return 1 + (1 + 2 * cut) + spmm
+        return spmm
 
     n_launch = sum(launches(k, kind) for k, kind, *_ in ops) * args.steps
 
