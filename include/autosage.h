@@ -119,7 +119,7 @@ typedef struct autosage_plan_s *autosage_plan_t;
 
 /* ---------------------------------------------------------------- ops */
 
-/* SpMM (Abstract: "CSR SpMM"). transpose == 0: Y[i,:] = sum_p vals[p] * X[col_idx[p],:]
+/* SpMM (Abstract: CSR SpMM). transpose == 0: Y[i,:] = sum_p vals[p] * X[col_idx[p],:]
  * for the n_rows rows of A; X has n_cols rows. transpose == 1: Y = A^T X, which needs a
  * plan built for AUTOSAGE_OP_SPMM_T (it holds A^T); Y has n_cols rows, X has n_rows rows.
  * dt is the type of X and Y (values, accumulation and softmax math are fp32).
@@ -128,20 +128,20 @@ autosage_status autosage_spmm(const autosage_csr *A, const void *X, int64_t ldx,
                               int64_t ldy, int64_t F, autosage_dtype dt, int transpose,
                               autosage_plan_t plan, void *stream);
 
-/* SDDMM (Abstract: "SDDMM"): out[p] = alpha * <Q[row(p),:], K[col_idx[p],:]> for every
+/* SDDMM (Abstract: SDDMM): out[p] = alpha * <Q[row(p),:], K[col_idx[p],:]> for every
  * edge p, written in CSR order as fp32 [nnz]. Edge values are not multiplied in.
  * Q has n_rows rows, K has n_cols rows, both of width F and type dt. */
 autosage_status autosage_sddmm(const autosage_csr *A, const void *Q, int64_t ldq, const void *K,
                                int64_t ldk, int64_t F, autosage_dtype dt, float alpha,
                                float *out, autosage_plan_t plan, void *stream);
 
-/* Row softmax of edge scores in place (Abstract: "row-softmax"; benchmark page: the row
+/* Row softmax of edge scores in place (Abstract: row-softmax; benchmark page: the row
  * maximum is subtracted first). scores is fp32 [nnz, heads]; each row and head is
  * normalised over the row's edges. */
 autosage_status autosage_row_softmax(const autosage_csr *A, float *scores, int heads,
                                      autosage_plan_t plan, void *stream);
 
-/* CSR attention (Abstract: "CSR attention pipeline (SDDMM -> row-softmax -> SpMM)"):
+/* CSR attention (Abstract: the pipeline SDDMM -> row-softmax -> SpMM):
  * per head h, s_p = scale * <Q[i,h,:], K[col_idx[p],h,:]>, w = softmax over row i,
  * out[i,h,:] = sum_p w_p V[col_idx[p],h,:]. Q/K/V/out are [n, heads, D] of type dt.
  * fused != 0: one pass per row with an online softmax; scores never reach HBM.

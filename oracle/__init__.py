@@ -133,7 +133,7 @@ def _matrix(X):
 
 
 def spmm(row_ptr, col_idx, vals, X, rows=None, heads: int = 1):
-    """Y = A X in double (Abstract: "CSR SpMM").
+    """Y = A X in double (Abstract: CSR SpMM).
 
     ``vals`` is [nnz] (or [nnz, heads] with ``heads > 1``) or None for all
     ones; X is [n_cols, heads * D]. Returns [len(rows) or n_rows, F] float64.
@@ -154,7 +154,7 @@ def spmm(row_ptr, col_idx, vals, X, rows=None, heads: int = 1):
 
 
 def sddmm(row_ptr, col_idx, Q, K, alpha: float = 1.0, heads: int = 1, rows=None):
-    """S[p, h] = alpha * <Q[row(p), h, :], K[col_idx[p], h, :]> in double (Abstract: "SDDMM").
+    """S[p, h] = alpha * <Q[row(p), h, :], K[col_idx[p], h, :]> in double (Abstract: SDDMM).
 
     Returns [nnz, heads] (or the edges of ``rows``, concatenated in order).
     """

@@ -33,7 +33,7 @@
 #define ROW(k) (rows ? rows[(k)] : (int64_t)(k))
 
 /* Y[i, h*D + d] = sum_{p in row i} vals[p*H + h] * X[col_idx[p], h*D + d].
- * H = 1 is plain SpMM Y = A X (Abstract: "CSR SpMM"); H > 1 aggregates each
+ * H = 1 is plain SpMM Y = A X (Abstract: CSR SpMM); H > 1 aggregates each
  * head with its own per-edge weight (the SpMM half of multi-head CSR
  * attention). vals == NULL means every weight is 1. */
 void oracle_spmm(int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
@@ -57,7 +57,7 @@ void oracle_spmm(int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
 }
 
 /* S[p*H + h] = alpha * sum_d Q[i, h*D + d] * K[col_idx[p], h*D + d] for every
- * edge p of row i (Abstract: "SDDMM"). Edge values are not multiplied in: the
+ * edge p of row i (Abstract: SDDMM). Edge values are not multiplied in: the
  * output is the dense product Q K^T sampled on the sparsity pattern. For a
  * row subset the edges of rows[0], rows[1], ... are written one after the
  * other into S (the caller sizes S from the row degrees). */
@@ -83,8 +83,8 @@ void oracle_sddmm(int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx
 }
 
 /* Row softmax of edge scores, per head: W[p,h] = exp(S[p,h] - m) / sum_q exp(S[q,h] - m)
- * with m the maximum of S[., h] over the row (benchmark page: "Find max for
- * numerical stability"). Rows are given by row_ptr; S and W hold
+ * with m the maximum of S[., h] over the row (benchmark page: the row maximum is
+ * subtracted first, for numerical stability). Rows are given by row_ptr; S and W hold
  * nnz * H entries. A row with no edges has nothing to write. */
 void oracle_row_softmax(int64_t n_rows, const int32_t *row_ptr, int64_t H,
                         const double *S, double *W) {
@@ -103,7 +103,7 @@ void oracle_row_softmax(int64_t n_rows, const int32_t *row_ptr, int64_t H,
   }
 }
 
-/* CSR attention (Abstract: "SDDMM -> row-softmax -> SpMM"), per head h:
+/* CSR attention (Abstract: the pipeline SDDMM -> row-softmax -> SpMM), per head h:
  *   s_p = scale * <Q[i,h,:], K[col_idx[p],h,:]>,   w_p = softmax over the row,
  *   O[i,h,:] = sum_p w_p * V[col_idx[p],h,:].
  * Scores stay in double (never rounded to float). Empty rows give zeros.

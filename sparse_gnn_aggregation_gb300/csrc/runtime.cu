@@ -2,9 +2,10 @@
 // workspace, the input-aware schedule picker (cost estimate from row
 // statistics, refined by on-device micro-probes), and the persistent plan
 // cache (AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN Aggregation
-// (SpMM/SDDMM) and CSR Attention", Abstract: "chooses tiling and mapping
-// per input using a lightweight estimate refined by on-device
-// micro-probes ... a persistent cache for deterministic replay"). The
+// (SpMM/SDDMM) and CSR Attention", Abstract: the scheduler picks tiling and
+// mapping for each input from a cheap cost estimate that short runs on the
+// device refine, and keeps its choices in a persistent cache so that later
+// runs replay them). The
 // fallback ("guardrail") is this library's own default row-group schedule,
 // never a vendor library or the CPU.
 #include <algorithm>

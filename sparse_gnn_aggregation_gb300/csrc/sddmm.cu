@@ -1,6 +1,6 @@
 // CSR SDDMM: S[p, h] = alpha * <Q[row(p), h, :], K[col_idx[p], h, :]>
 // (AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN Aggregation
-// (SpMM/SDDMM) and CSR Attention", Abstract: "SDDMM"; the first step of the
+// (SpMM/SDDMM) and CSR Attention", Abstract: SDDMM; the first step of the
 // CSR attention pipeline). Edge values of A are not multiplied in.
 //
 // A lane group owns a row (or a chunk of a cut row): its G feature lanes hold

@@ -1,7 +1,7 @@
 // CSR SpMM kernels: Y = A X (AutoSAGE, "Input-Aware CUDA Scheduling for
-// Sparse GNN Aggregation (SpMM/SDDMM) and CSR Attention", Abstract: "CSR
-// SpMM"), with per-head edge weights for the aggregation step of CSR
-// attention (Abstract: "SDDMM -> row-softmax -> SpMM").
+// Sparse GNN Aggregation (SpMM/SDDMM) and CSR Attention", Abstract: CSR
+// SpMM), with per-head edge weights for the aggregation step of CSR
+// attention (Abstract: the pipeline SDDMM -> row-softmax -> SpMM).
 //
 // The work is a gather: every edge reads one source row of X. Kernels are
 // HBM-bound; they use no tensor cores. Three schedules:
