@@ -35,3 +35,30 @@ def test_algorithmic_bytes():
     ops = bench.op_list({"rmat": None, "uniform": None})
     assert len(ops) == 2 * 2 * len(bench.FS) + 3
     assert [k for k, *_ in ops][-3:] == ["spmm_t/rmat/F64", "attn_fused/rmat/H8D64", "attn_unfused/rmat/H8D64"]
+
+
+def test_cache_aware_bound():
+    gp = {"l2_GBps": 20000.0, "dram_GBps": 8000.0}
+    # DRAM side: 8 GB of DRAM bytes at 8 TB/s is 1 ms; 10 GB through L2 at 20 TB/s is 0.5 ms
+    bound, frac = bench.cache_bound(10e9, 8e9, 2.0, gp)
+    assert bound == 1.0 and frac == 0.5
+    # L2 side: 40 GB through L2 at 20 TB/s is 2 ms, more than 1 ms of DRAM
+    bound, frac = bench.cache_bound(40e9, 8e9, 4.0, gp)
+    assert bound == 2.0 and frac == 0.5
+    # no DRAM count or no measured rates: no bound
+    assert bench.cache_bound(10e9, None, 2.0, gp) == (None, None)
+    assert bench.cache_bound(10e9, 8e9, 2.0, None) == (None, None)
+
+
+def test_roofline_entry_fields(monkeypatch):
+    per_op = {"attn_fused/rmat/H8D64": {"ms": 2.0}}
+    monkeypatch.setattr(bench, "traffic_for", lambda key: 4e9)
+    gp = {"l2_GBps": 20000.0, "dram_GBps": 8000.0, "row_bytes": 2048}
+    e = bench.roofline_entry("attn_fused/rmat/H8D64", per_op, 10000.0, 6746.6, "measured", gp)
+    assert e["bound"] == "hbm" and e["unit"] == "GB/s" and e["peak"] == 6746.6
+    assert e["frac"] == round(10000.0 / 6746.6, 4)
+    assert e["traffic"] == 4e9 and e["traffic_GBps"] == 2000.0
+    assert e["l2_frac"] == 0.5
+    # 20 GB of algorithmic bytes: 1 ms through L2, 0.5 ms of DRAM -> bound 1 ms of 2 ms
+    assert e["cache_aware_bound_ms"] == 1.0 and e["cache_aware_frac"] == 0.5
+    assert "gather_peaks" not in bench.roofline_entry("attn_fused/rmat/H8D64", per_op, 10000.0, 6746.6, "measured")
