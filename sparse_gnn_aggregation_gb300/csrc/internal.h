@@ -41,6 +41,12 @@ cudaError_t launch_spmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                         void *Y, int64_t ldy, const ChunkList &cl, float *partial,
                         cudaStream_t s);
 
+// Two SpMMs over one CSR in one pass: Y1 = A_vals1 X1 and Y2 = A_vals2 X2
+// (same geometry and leading dimensions); partial: [2 * n_chunks * F] fp32.
+cudaError_t launch_spmm2(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
+                         const float *vals1, const float *vals2, const void *X1, const void *X2, int64_t ldx,
+                         void *Y1, void *Y2, int64_t ldy, const ChunkList &cl, float *partial, cudaStream_t s);
+
 // SDDMM: S[p*H + h] = alpha * <Q[row, h], K[col, h]>. Items come from the
 // chunk list's deal, or (mp_part != null) from a merge path: lane group w
 // takes diagonals [mp_part[w], mp_part[w + 1]) of the (rows + edges) path,

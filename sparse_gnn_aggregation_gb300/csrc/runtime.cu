@@ -696,20 +696,22 @@ autosage_status run_op(const autosage_plan_s *P, autosage_op op, const autosage_
                                     a.alpha, a.dQ, P->scores.as<float>(), P->grad_dw.as<float>(),
                                     P->t_inv.as<int32_t>(), P->grad_wt.as<float>(), P->grad_dst.as<float>(), cl,
                                     P->partial.as<float>(), P->row_ml.as<float>(), s);
-      // dV = SpMM(A^T; w, dO), dK = SpMM(A^T; scale * dS, Q)
+      // dV = SpMM(A^T; w, dO) and dK = SpMM(A^T; scale * dS, Q) in one pass over A^T
       if (e == cudaSuccess) {
-        st = choose_geom(P->dt, P->H, P->F, {{a.dO, ld}, {a.dV, ld}}, T->sched.G, T->sched.E, false, 16, g);
+        st = choose_geom(P->dt, P->H, P->F, {{a.dO, ld}, {a.dV, ld}, {a.Q, ld}, {a.dK, ld}}, T->sched.G,
+                         T->sched.E, false, 16, g);
         if (st != AUTOSAGE_OK) return st;
         g.comp = T->comp;
-        e = launch_spmm(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_wt.as<float>(), a.dO, ld, a.dV, ld,
-                        T->cl, T->partial.as<float>(), s);
-      }
-      if (e == cudaSuccess) {
-        st = choose_geom(P->dt, P->H, P->F, {{a.Q, ld}, {a.dK, ld}}, T->sched.G, T->sched.E, false, 16, g);
-        if (st != AUTOSAGE_OK) return st;
-        g.comp = T->comp;
-        e = launch_spmm(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_dst.as<float>(), a.Q, ld, a.dK, ld,
-                        T->cl, T->partial.as<float>(), s);
+        if (g.NV <= 4) {
+          e = launch_spmm2(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_wt.as<float>(),
+                           P->grad_dst.as<float>(), a.dO, a.Q, ld, a.dV, a.dK, ld, T->cl, T->partial.as<float>(), s);
+        } else {  // rows of more than 4 fragments a lane: two products spill, so two passes
+          e = launch_spmm(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_wt.as<float>(), a.dO, ld, a.dV, ld,
+                          T->cl, T->partial.as<float>(), s);
+          if (e == cudaSuccess)
+            e = launch_spmm(g, T->k_rows, T->k_row_ptr, T->k_col_idx, P->grad_dst.as<float>(), a.Q, ld, a.dK, ld,
+                            T->cl, T->partial.as<float>(), s);
+        }
       }
       break;
     }
@@ -1150,6 +1152,14 @@ autosage_status build_backward_plan(autosage_plan_s *P, const Sched &sc, cudaStr
   if (st != AUTOSAGE_OK) {
     delete T;
     return st;
+  }
+  // dV and dK run as one two-product pass: partials of both outputs for cut rows
+  if (T->cl.n_chunks > 0) {
+    const cudaError_t e = T->partial.alloc(sizeof(float) * (size_t)(2 * (int64_t)T->cl.n_chunks * T->F));
+    if (e != cudaSuccess) {
+      delete T;
+      return cuda_fail(e, "backward partials");
+    }
   }
   delete P->tplan;
   P->tplan = T;

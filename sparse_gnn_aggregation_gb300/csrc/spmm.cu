@@ -113,6 +113,64 @@ __device__ __forceinline__ void gather_edges(const int32_t *__restrict__ col_idx
   }
 }
 
+// Two products over the same edges in one walk: acc1 += w1 * X1[col] and
+// acc2 += w2 * X2[col] (per-head weights vals1, vals2 with the same layout).
+// Each edge's column is loaded once and both rows are in flight together;
+// each sum takes its edges in the order gather_edges would, so both outputs
+// have the bits of two separate SpMMs.
+template <typename T, int VW, int NV, int U, bool COMP>
+__device__ __forceinline__ void gather_edges2(const int32_t *__restrict__ col_idx, const float *__restrict__ vals1,
+                                              const float *__restrict__ vals2, int H, int es, bool one,
+                                              const int (&head)[NV], const T *__restrict__ X1,
+                                              const T *__restrict__ X2, int64_t ldx, int nfrag,
+                                              const int (&frag)[NV], int E, int p0, int pe,
+                                              float (&acc1)[NV][VW], float (&comp1)[NV][VW],
+                                              float (&acc2)[NV][VW], float (&comp2)[NV][VW]) {
+  if (p0 >= pe) return;
+  int c[U];
+  float w1[U][NV], w2[U][NV];
+  load_weights<U, NV>(col_idx, vals1, H, es, one, head, p0, E, pe, c, w1);
+  load_weights<U, NV>(col_idx, vals2, H, es, one, head, p0, E, pe, c, w2);
+  for (int p = p0; p < pe; p += U * E) {
+    Frag<T, VW> f1[U][NV], f2[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (p + u * E < pe && frag[k] < nfrag) {
+          f1[u][k].load(X1 + (int64_t)c[u] * ldx + (int64_t)frag[k] * VW);
+          f2[u][k].load(X2 + (int64_t)c[u] * ldx + (int64_t)frag[k] * VW);
+        }
+    const int pn = p + U * E;
+    int cn[U];
+    float wn1[U][NV], wn2[U][NV];
+    if (pn < pe) {
+      load_weights<U, NV>(col_idx, vals1, H, es, one, head, pn, E, pe, cn, wn1);
+      load_weights<U, NV>(col_idx, vals2, H, es, one, head, pn, E, pe, cn, wn2);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (p + u * E < pe)
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+          if (frag[k] < nfrag)
+#pragma unroll
+            for (int v = 0; v < VW; ++v) {
+              accum<COMP>(acc1[k][v], comp1[k][v], w1[u][k], f1[u][k].get(v));
+              accum<COMP>(acc2[k][v], comp2[k][v], w2[u][k], f2[u][k].get(v));
+            }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      c[u] = cn[u];
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        w1[u][k] = wn1[u][k];
+        w2[u][k] = wn2[u][k];
+      }
+    }
+  }
+}
+
 // gather_edges over column indices and weights staged in shared memory (sc,
 // sv: entries for the edges from `base` on; sv null: weight 1): the same
 // rounds and the same order of additions, with the index and weight loads
@@ -197,6 +255,73 @@ __global__ void __launch_bounds__(kBlock) spmm_rows_kernel(
 #pragma unroll
       for (int k = 0; k < NV; ++k)
         if (frag[k] < nfrag) store_partial<VW>(y + (int64_t)frag[k] * VW, acc[k]);
+    }
+  }
+}
+
+// Two SpMMs over one CSR in one pass (Y1 = A_w1 X1, Y2 = A_w2 X2; the edge
+// weights differ, the structure is shared): the attention backward's dV and
+// dK over the rows of A^T. Cut rows write both partials (partial and
+// partial + n_chunks * F).
+// Blocks per SM the two-product kernel is sized for: three 256-thread blocks
+// (80 registers) where a lane holds few values, with one edge per round for
+// both products (measured on the attention backward, R-MAT scale 20, bf16,
+// H = 8, D = 64: 11.64 ms against 11.73 ms for two edges per round at two
+// blocks, and 11.99 ms for two separate SpMMs).
+// Narrower fragments and compensated sums spilled at that bound, so they keep
+// the registers they need.
+template <typename T, int VW, int NV, bool COMP>
+constexpr int spmm2_min_blocks() {
+  return (!COMP && VW * sizeof(T) == 16 && (NV * VW <= 4 || (sizeof(T) == 2 && NV * VW <= 16))) ? 3 : 1;
+}
+
+template <typename T, int VW, int NV, bool COMP>
+__global__ void __launch_bounds__(kBlock, spmm2_min_blocks<T, VW, NV, COMP>()) spmm2_rows_kernel(
+    int64_t n_rows, const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
+    const float *__restrict__ vals1, const float *__restrict__ vals2, int H, int es, int cph,
+    const T *__restrict__ X1, const T *__restrict__ X2, int64_t ldx, T *__restrict__ Y1, T *__restrict__ Y2,
+    int64_t ldy, int nfrag, int G, int E, int fs, int ks, bool one, ChunkList cl, int ipb,
+    float *__restrict__ partial) {
+  const Lanes L(G, E);
+  int frag[NV], head[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    frag[k] = L.g * fs + k * ks;
+    head[k] = (H > 1 && frag[k] < nfrag) ? frag[k] / cph : 0;
+  }
+  const int64_t F = (int64_t)nfrag * VW;
+  __shared__ int s_items;
+  const ItemQueue queue(n_rows, cl, ipb, &s_items);
+  int64_t idx;
+  while (queue.next(L, idx)) {
+    const Item it = item_at(idx, n_rows, row_ptr, cl);
+    float acc1[NV][VW], comp1[NV][VW], acc2[NV][VW], comp2[NV][VW];
+    zero(acc1);
+    zero(comp1);
+    zero(acc2);
+    zero(comp2);
+    gather_edges2<T, VW, NV, (unroll_for<NV, VW>() > 1 ? unroll_for<NV, VW>() / 2 : 1), COMP>(col_idx, vals1, vals2, H, es, one, head, X1, X2, ldx,
+                                                          nfrag, frag, E, it.b + L.e, it.e, acc1, comp1, acc2,
+                                                          comp2);
+    reduce_edge_lanes(acc1, L.group_mask, G, L.GE);
+    reduce_edge_lanes(acc2, L.group_mask, G, L.GE);
+    if (!it.active || L.e != 0) continue;
+    if (it.chunk < 0) {
+      T *y1 = Y1 + it.row * ldy, *y2 = Y2 + it.row * ldy;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (frag[k] < nfrag) {
+          store_frag<T, VW>(y1 + (int64_t)frag[k] * VW, acc1[k]);
+          store_frag<T, VW>(y2 + (int64_t)frag[k] * VW, acc2[k]);
+        }
+    } else {
+      float *p1 = partial + (int64_t)it.chunk * F, *p2 = partial + ((int64_t)cl.n_chunks + it.chunk) * F;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (frag[k] < nfrag) {
+          store_partial<VW>(p1 + (int64_t)frag[k] * VW, acc1[k]);
+          store_partial<VW>(p2 + (int64_t)frag[k] * VW, acc2[k]);
+        }
     }
   }
 }
@@ -512,6 +637,44 @@ cudaError_t spmm_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const
 }
 
 template <typename T, int VW>
+cudaError_t spmm2_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
+                     const float *vals1, const float *vals2, const T *X1, const T *X2, int64_t ldx, T *Y1, T *Y2,
+                     int64_t ldy, const ChunkList &cl_in, float *partial, cudaStream_t s) {
+  const Deal dl = deal_items(cl_in, n_rows, g.G * g.E, g.G);
+  const ChunkList &cl = dl.cl;
+  const int ipb = dl.ipb;
+  const int64_t grid = dl.grid;
+  if (grid > 0) {
+#define AUTOSAGE_SPMM2_K(NVV, CMP)                                                                    \
+  spmm2_rows_kernel<T, VW, NVV, CMP><<<(unsigned)grid, kBlock, 0, s>>>(                              \
+      n_rows, row_ptr, col_idx, vals1, vals2, g.H, g.es, g.cph, X1, X2, ldx, Y1, Y2, ldy, g.nfrag, g.G, g.E, \
+      g.fs, g.ks, g.one, cl, ipb, partial)
+#define AUTOSAGE_SPMM2_NV(NVV)          \
+  if (g.comp) AUTOSAGE_SPMM2_K(NVV, true); \
+  else AUTOSAGE_SPMM2_K(NVV, false);
+    switch (g.NV) {
+      case 1: AUTOSAGE_SPMM2_NV(1); break;
+      case 2: AUTOSAGE_SPMM2_NV(2); break;
+      case 4: AUTOSAGE_SPMM2_NV(4); break;
+      case 8: AUTOSAGE_SPMM2_NV(8); break;
+      default: return cudaErrorInvalidValue;
+    }
+#undef AUTOSAGE_SPMM2_NV
+#undef AUTOSAGE_SPMM2_K
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (cl.n_long > 0) {
+    const unsigned fgrid = (unsigned)((cl.n_long + kBlock / 32 - 1) / (kBlock / 32));
+    const int64_t F = (int64_t)g.nfrag * g.VW;
+    spmm_fixup_kernel<T, VW><<<fgrid, kBlock, 0, s>>>(cl, g.nfrag, partial, Y1, ldy);
+    spmm_fixup_kernel<T, VW><<<fgrid, kBlock, 0, s>>>(cl, g.nfrag, partial + (int64_t)cl.n_chunks * F, Y2, ldy);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+template <typename T, int VW>
 cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                          const int32_t *col_idx, const float *vals, const T *X, int64_t ldx, T *Y,
                          int64_t ldy, const int2 *part, int64_t n_warps, int items, float *carry_val,
@@ -548,6 +711,30 @@ cudaError_t mergepath_vw(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
 }
 
 }  // namespace
+
+cudaError_t launch_spmm2(const Geom &g, int64_t n_rows, const int32_t *row_ptr, const int32_t *col_idx,
+                         const float *vals1, const float *vals2, const void *X1, const void *X2, int64_t ldx,
+                         void *Y1, void *Y2, int64_t ldy, const ChunkList &cl, float *partial, cudaStream_t s) {
+  if (g.dt == DType::F32) {
+    auto x1 = static_cast<const float *>(X1), x2 = static_cast<const float *>(X2);
+    auto y1 = static_cast<float *>(Y1), y2 = static_cast<float *>(Y2);
+    switch (g.VW) {
+      case 4: return spmm2_vw<float, 4>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+      case 2: return spmm2_vw<float, 2>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+      case 1: return spmm2_vw<float, 1>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+    }
+  } else {
+    auto x1 = static_cast<const __nv_bfloat16 *>(X1), x2 = static_cast<const __nv_bfloat16 *>(X2);
+    auto y1 = static_cast<__nv_bfloat16 *>(Y1), y2 = static_cast<__nv_bfloat16 *>(Y2);
+    switch (g.VW) {
+      case 8: return spmm2_vw<__nv_bfloat16, 8>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+      case 4: return spmm2_vw<__nv_bfloat16, 4>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+      case 2: return spmm2_vw<__nv_bfloat16, 2>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+      case 1: return spmm2_vw<__nv_bfloat16, 1>(g, n_rows, row_ptr, col_idx, vals1, vals2, x1, x2, ldx, y1, y2, ldy, cl, partial, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_spmm(const Geom &g, int64_t n_rows, const int32_t *row_ptr,
                         const int32_t *col_idx, const float *vals, const void *X, int64_t ldx,

@@ -83,3 +83,10 @@ def test_backward_repeat_is_bitwise_identical():
         again = sga.autosage_csr_attention_backward(A, *x, H, 0.25, plan=plan)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+
+
+# wide rows: 4 fragments a lane (dV and dK in one pass over A^T) and 8 (two passes)
+@pytest.mark.parametrize("H,D", [(2, 256), (4, 256)])
+@pytest.mark.parametrize("schedule", [None, dict(kind=sga.SCHED_SPLIT, split=16)], ids=["auto", "split16"])
+def test_backward_wide_rows(H, D, schedule):
+    run(synth.rmat_skew(10, seed=6), H, D, 1 / np.sqrt(D), 5, schedule=schedule)
