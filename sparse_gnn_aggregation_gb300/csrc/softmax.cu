@@ -49,7 +49,17 @@ __global__ void __launch_bounds__(kBlock) softmax_rows_kernel(int64_t n_rows,
   const Item it = item_at(idx, n_rows, row_ptr, cl);
   const int64_t i0 = (int64_t)it.b * H, i1 = (int64_t)it.e * H;
   ML a{-INFINITY, 0.f};
-  for (int64_t i = i0 + L.g; i < i1; i += GS) ml_add(a, S[i]);
+  // four scores a lane in flight at a time, taken in the lane's order (the
+  // same bits as one at a time; unfused attention on R-MAT scale 20, bf16,
+  // H = 8, D = 64: 5.80 -> 5.63 ms)
+  for (int64_t i = i0 + L.g; i < i1; i += 4 * GS) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = i + u * GS < i1 ? S[i + u * GS] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * GS < i1) ml_add(a, x[u]);
+  }
   for (int off = H; off < GS; off <<= 1) {
     ML b{__shfl_xor_sync(L.group_mask, a.m, off), __shfl_xor_sync(L.group_mask, a.l, off)};
     a = ml_merge(a, b);
@@ -64,7 +74,14 @@ __global__ void __launch_bounds__(kBlock) softmax_rows_kernel(int64_t n_rows,
     continue;
   }
   const float inv = a.l > 0.f ? 1.f / a.l : 0.f;
-  for (int64_t i = i0 + L.g; i < i1; i += GS) S[i] = __expf(S[i] - a.m) * inv;
+  for (int64_t i = i0 + L.g; i < i1; i += 4 * GS) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = i + u * GS < i1 ? S[i + u * GS] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * GS < i1) S[i + u * GS] = __expf(x[u] - a.m) * inv;
+  }
   }
 }
 
