@@ -191,12 +191,14 @@ def attn_backward_bytes(n, m, nnz, H, D, s):
     rows of A (CSR arrays, Q and dO rows once per row, K and V rows gathered
     per edge, dQ written, scores and dW written and read back per edge and
     head, the A^T position of each edge read, w and dS written in A^T order)
-    and the two SpMMs over A^T for dV and dK (per-head weights, gathered dO
-    and Q rows, outputs)."""
+    and the two SpMMs over A^T for dV and dK (A^T's CSR arrays once, then for
+    each product its per-head weights, its gathered dO or Q rows and its
+    output)."""
     W = H * D
     rows = 4 * (n + 1) + 4 * nnz + 3 * n * W * s + 2 * nnz * W * s + 4 * 4 * nnz * H + 4 * nnz + 2 * 4 * nnz * H
-    spmm_t = 4 * (m + 1) + 4 * nnz + 4 * nnz * H + nnz * W * s + m * W * s
-    return rows + 2 * spmm_t
+    csr_t = 4 * (m + 1) + 4 * nnz
+    product = 4 * nnz * H + nnz * W * s + m * W * s
+    return rows + csr_t + 2 * product
 
 
 def workload_config(graphs, world):

@@ -62,3 +62,12 @@ def test_roofline_entry_fields(monkeypatch):
     # 20 GB of algorithmic bytes: 1 ms through L2, 0.5 ms of DRAM -> bound 1 ms of 2 ms
     assert e["cache_aware_bound_ms"] == 1.0 and e["cache_aware_frac"] == 0.5
     assert "gather_peaks" not in bench.roofline_entry("attn_fused/rmat/H8D64", per_op, 10000.0, 6746.6, "measured")
+
+
+def test_backward_bytes_count_the_transpose_structure_once():
+    n, m, nnz, H, D, s = 10, 12, 100, 2, 8, 2
+    W = H * D
+    rows = 4 * (n + 1) + 4 * nnz + 3 * n * W * s + 2 * nnz * W * s + 16 * nnz * H + 4 * nnz + 8 * nnz * H
+    # A^T's row_ptr and col_idx once; per product: weights, gathered rows, output rows
+    want = rows + 4 * (m + 1) + 4 * nnz + 2 * (4 * nnz * H + nnz * W * s + m * W * s)
+    assert bench.attn_backward_bytes(n, m, nnz, H, D, s) == want
