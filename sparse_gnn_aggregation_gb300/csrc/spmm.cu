@@ -489,7 +489,11 @@ __global__ void __launch_bounds__(kBlock, mp_min_blocks<VW, NV, STAGED>()) spmm_
 
 // The first warp carrying a row adds every carry of that row (in warp order)
 // and then the fp32 segment of the row's finishing warp (the warp after the
-// last carry), and rounds the sum to T once.
+// last carry), and rounds the sum to T once. The run of warps carrying the
+// row is found 32 at a time with a ballot, and four carries are loaded ahead
+// of their additions (a hub row of the skewed graph is carried by a hundred
+// warps and more; loading them one by one, each behind the test for the next
+// warp's row, made this the merge path's long tail).
 template <typename T, int VW>
 __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
     int64_t n_warps, int nfrag, const float *__restrict__ carry_val,
@@ -500,6 +504,18 @@ __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
   const int r = carry_row[w];
   if (r < 0 || (w > 0 && carry_row[w - 1] == r)) return;
   const int lane = threadIdx.x & 31;
+  // warps w .. q_end - 1 carry row r
+  int64_t q_end = w + 1;
+  for (;;) {
+    const int64_t q = q_end + lane;
+    const bool same = q < n_warps && carry_row[q] == r;
+    const unsigned other = __ballot_sync(FULL, !same);
+    if (other) {
+      q_end += __ffs(other) - 1;
+      break;
+    }
+    q_end += 32;
+  }
   const int64_t F = (int64_t)nfrag * VW;
   for (int f = lane; f < nfrag; f += 32) {
     float acc[VW];
@@ -509,14 +525,25 @@ __global__ void __launch_bounds__(kBlock) mergepath_fixup_kernel(
 #pragma unroll
     for (int v = 0; v < VW; ++v) comp[v] = 0.f;
     int64_t q = w;
-    for (; q < n_warps && carry_row[q] == r; ++q) {
+    for (; q + 4 <= q_end; q += 4) {
+      float x[4][VW];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < VW; ++v) x[u][v] = __ldcg(carry_val + (q + u) * F + (int64_t)f * VW + v);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, x[u][v]);
+    }
+    for (; q < q_end; ++q) {
       const float *src = carry_val + q * F + (int64_t)f * VW;
 #pragma unroll
       for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, __ldcg(src + v));
     }
-    // warp q finishes row r (a carried row always ends in a later warp, so q < n_warps)
-    if (q < n_warps) {
-      const float *hv = head_val + q * F + (int64_t)f * VW;
+    // warp q_end finishes row r (a carried row always ends in a later warp, so q_end < n_warps)
+    if (q_end < n_warps) {
+      const float *hv = head_val + q_end * F + (int64_t)f * VW;
 #pragma unroll
       for (int v = 0; v < VW; ++v) accum<true>(acc[v], comp[v], 1.f, __ldcg(hv + v));
     }
