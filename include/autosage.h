@@ -4,9 +4,10 @@
  * Operations follow AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN
  * Aggregation (SpMM/SDDMM) and CSR Attention" (Abstract): CSR SpMM, SDDMM,
  * and the CSR attention pipeline SDDMM -> row-softmax -> SpMM, each run by
- * a schedule that an input-aware planner picks with a cost estimate refined
- * by on-device micro-probes and keeps in a persistent cache for
- * deterministic replay. The graph interface follows the benchmark page
+ * a schedule that an input-aware planner picks from a cost estimate, checks
+ * with short timed runs on the device, and stores in a persistent cache so
+ * that later runs reuse the same choice. The graph interface follows the
+ * benchmark page
  * "fused sparse attention-value aggregation" (problem statement): rows are
  * destination nodes, row_ptr has n_rows + 1 int32 entries, col_idx holds
  * each edge's source node, an edgeless row produces zeros.

@@ -1,6 +1,6 @@
 // Host runtime and C ABI: argument checks, feature geometry, plans and their
 // workspace, the input-aware schedule picker (cost estimate from row
-// statistics, refined by on-device micro-probes), and the persistent plan
+// statistics, checked by short timed runs on the device), and the persistent plan
 // cache (AutoSAGE, "Input-Aware CUDA Scheduling for Sparse GNN Aggregation
 // (SpMM/SDDMM) and CSR Attention", Abstract: the scheduler picks tiling and
 // mapping for each input from a cheap cost estimate that short runs on the
